@@ -1,0 +1,179 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the smoke check.
+
+This module holds no attention arithmetic: it only draws random numbers, rounds
+them to bf16 and lays out paged caches and block tables. Both the CUDA path and
+the CPU oracle are fed from here; neither is imported by it.
+
+Recipe (one ``torch.Generator`` on the CPU per call, seeded explicitly):
+
+* prefill: q, k, v drawn in that order, iid N(0, 1) in fp32, rounded to bf16
+  (round-to-nearest-even). Optional "boosted" keys: per (b, kv head) slice, a
+  seeded choice of ``floor(frac * Nk)`` distinct token rows of K is multiplied
+  by ``boost`` (2.0 is exact in bf16). This forces late running-max rises.
+* decode: sequence lengths uniform integers in [len_lo, len_hi], then a random
+  permutation of the ``sum(ceil(L / block_size))`` physical blocks (plus
+  ``extra_blocks`` unused ones), then q, then the K cache, then the V cache,
+  iid N(0, 1) rounded to bf16. The block table lists each sequence's physical
+  blocks in logical order; unused entries are -1. ``poison`` fills every cache
+  slot that no sequence owns (tail slots of a last block, unused blocks) with NaN.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+# Head dimension and tile sizes every path supports.
+SUPPORTED_HEAD_DIMS = (64, 128)
+
+
+@dataclass(frozen=True)
+class PrefillConfig:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    window: int = -1          # keys allowed left of the diagonal; -1 = unlimited
+    k_boost_frac: float = 0.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+@dataclass(frozen=True)
+class DecodeConfig:
+    name: str
+    num_seqs: int
+    Hq: int
+    Hkv: int
+    d: int
+    block_size: int
+    len_lo: int
+    len_hi: int
+    seed: int = 0
+    extra_blocks: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# The five workloads (shapes of the pages' examples: N=512/d=64 single head;
+# 2k and 8k causal prefill with d=128; GQA with 4 query heads per kv head and a
+# sliding window; paged GQA decode with 16-token pages and up to 32k context).
+C1 = PrefillConfig("C1_single_head_noncausal_N512_d64", 1, 1, 1, 512, 512, 64, False)
+C2 = PrefillConfig("C2_causal_B4_H16_N2048_d128", 4, 16, 16, 2048, 2048, 128, True)
+C3 = PrefillConfig("C3_long_causal_B1_H32_N8192_d128_boost1pct", 1, 32, 32, 8192, 8192, 128, True,
+                   k_boost_frac=0.01)
+C4 = PrefillConfig("C4_gqa_causal_window1024_B2_Hq32_Hkv8_N4096_d128", 2, 32, 8, 4096, 4096, 128, True,
+                   window=1024)
+C5 = DecodeConfig("C5_paged_gqa_decode_S64_Hq32_Hkv8_d128_bs16_L1k_32k", 64, 32, 8, 128, 16, 1024, 32768)
+
+PREFILL_CONFIGS = {c.name: c for c in (C1, C2, C3, C4)}
+DECODE_CONFIGS = {C5.name: C5}
+
+
+def _bf16_normal(gen: torch.Generator, shape) -> torch.Tensor:
+    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+
+def prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=0, k_boost_frac=0.0, k_boost=2.0):
+    """Return host bf16 tensors q [B][Hq][Nq][d], k, v [B][Hkv][Nk][d]."""
+    gen = torch.Generator().manual_seed(int(seed))
+    q = _bf16_normal(gen, (B, Hq, Nq, d))
+    k = _bf16_normal(gen, (B, Hkv, Nk, d))
+    v = _bf16_normal(gen, (B, Hkv, Nk, d))
+    n_boost = int(math.floor(k_boost_frac * Nk))
+    if n_boost > 0:
+        for b in range(B):
+            for h in range(Hkv):
+                rows = torch.randperm(Nk, generator=gen)[:n_boost]
+                k[b, h, rows] = (k[b, h, rows].float() * k_boost).to(torch.bfloat16)
+    return q, k, v
+
+
+def prefill_config_inputs(cfg: PrefillConfig, seed=None):
+    return prefill_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.Nq, cfg.Nk, cfg.d,
+                          seed=cfg.seed if seed is None else seed, k_boost_frac=cfg.k_boost_frac)
+
+
+@dataclass
+class PagedDecodeInputs:
+    q: torch.Tensor            # [S][Hq][d] bf16
+    k_cache: torch.Tensor      # [num_blocks][Hkv][bs][d] bf16
+    v_cache: torch.Tensor
+    block_table: torch.Tensor  # [S][max_blocks] int32, -1 = unused
+    seq_lens: torch.Tensor     # [S] int32
+    block_size: int
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def kv_bytes(self) -> int:
+        """Bytes of K and V that the sequences own (every token, both caches)."""
+        Hkv, d = self.k_cache.shape[1], self.k_cache.shape[3]
+        return int(self.seq_lens.to(torch.int64).sum()) * Hkv * d * 2 * 2
+
+
+def decode_inputs(num_seqs, Hq, Hkv, d, block_size, seq_lens=None, len_lo=1, len_hi=1, seed=0,
+                  extra_blocks=0, max_blocks_per_seq=None, poison=False, identity_table=False,
+                  chunk_blocks=4096):
+    """Paged decode inputs. ``seq_lens`` (list) overrides the drawn lengths."""
+    gen = torch.Generator().manual_seed(int(seed))
+    if seq_lens is None:
+        lens = torch.randint(len_lo, len_hi + 1, (num_seqs,), generator=gen, dtype=torch.int64)
+    else:
+        lens = torch.as_tensor(list(seq_lens), dtype=torch.int64)
+        assert lens.numel() == num_seqs
+    nblk = [(int(L) + block_size - 1) // block_size for L in lens]
+    used = sum(nblk)
+    num_blocks = max(used + int(extra_blocks), 1)
+    if identity_table:
+        perm = torch.arange(num_blocks, dtype=torch.int64)
+    else:
+        perm = torch.randperm(num_blocks, generator=gen)
+    mb = max(nblk) if nblk else 0
+    if max_blocks_per_seq is not None:
+        assert max_blocks_per_seq >= mb
+        mb = max_blocks_per_seq
+    mb = max(mb, 1)
+    table = torch.full((num_seqs, mb), -1, dtype=torch.int32)
+    pos = 0
+    for s, n in enumerate(nblk):
+        table[s, :n] = perm[pos:pos + n].to(torch.int32)
+        pos += n
+    q = _bf16_normal(gen, (num_seqs, Hq, d))
+    caches = []
+    for _ in range(2):
+        c = torch.empty((num_blocks, Hkv, block_size, d), dtype=torch.bfloat16)
+        for b0 in range(0, num_blocks, chunk_blocks):
+            b1 = min(num_blocks, b0 + chunk_blocks)
+            c[b0:b1] = _bf16_normal(gen, (b1 - b0, Hkv, block_size, d))
+        caches.append(c)
+    k_cache, v_cache = caches
+    if poison:
+        owned = torch.zeros((num_blocks, block_size), dtype=torch.bool)
+        for s in range(num_seqs):
+            L = int(lens[s])
+            for lb in range(nblk[s]):
+                phys = int(table[s, lb])
+                n_tok = min(block_size, L - lb * block_size)
+                owned[phys, :n_tok] = True
+        nan = torch.tensor(float("nan"), dtype=torch.bfloat16)
+        mask = ~owned  # [num_blocks][bs]
+        for c in (k_cache, v_cache):
+            c.masked_fill_(mask[:, None, :, None], nan)
+    return PagedDecodeInputs(q=q, k_cache=k_cache, v_cache=v_cache, block_table=table,
+                             seq_lens=lens.to(torch.int32), block_size=block_size)
+
+
+def decode_config_inputs(cfg: DecodeConfig, seed=None, poison=False):
+    return decode_inputs(cfg.num_seqs, cfg.Hq, cfg.Hkv, cfg.d, cfg.block_size, len_lo=cfg.len_lo,
+                         len_hi=cfg.len_hi, seed=cfg.seed if seed is None else seed,
+                         extra_blocks=cfg.extra_blocks, poison=poison)

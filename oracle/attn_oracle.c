@@ -1,0 +1,435 @@
+/*
+ * Exact scaled-dot-product attention: plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark may load this file's library. The product path (the CUDA
+ * library and its Python binding) never calls it, shares no code with it and
+ * never falls back to it.
+ *
+ * Everything here is written for a reader checking it against the pages by eye:
+ * no tiling beyond what a function's definition states, no fusion, no reordering.
+ * All arithmetic is in double precision. Inputs are double arrays (callers pass
+ * the bf16 values the GPU sees, widened exactly to double).
+ *
+ * Pages cited (by title and section):
+ *   [MAK]  "Modern attention kernels" (blog.ecitis.org)
+ *   [FAV]  "Flash attention" (understandingdata.com, AI engineering visualised)
+ *   [IOA]  "Flash attention and IO-aware attention" (aigrafen.se)
+ *   [AK]   "Attention kernels" (inference.tusharamrit.in)
+ *
+ * Layouts (row-major, contiguous):
+ *   q, o : [B][Hq][Nq][d]      k, v : [B][Hkv][Nk][d]      lse : [B][Hq][Nq]
+ *   paged caches : [num_blocks][Hkv][block_size][d]
+ *   block_table  : int32 [num_seqs][max_blocks_per_seq]
+ *
+ * Readings taken where the pages are silent:
+ *   - causal alignment is bottom-right: row i may see key j iff j <= i + (Nk - Nq);
+ *   - window w >= 0 adds the left limit j >= i + (Nk - Nq) - w (w < 0: no limit);
+ *   - query head h reads kv head h / (Hq / Hkv) (contiguous groups);
+ *   - a row with no allowed key has O = 0 and lse = -inf;
+ *   - lse is the natural log of the sum of exp over the scaled scores.
+ *
+ * Every function returns 0 on success and a negative value on invalid arguments.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+#define ORACLE_ENOMEM (-2)
+#define ORACLE_EBOUNDS (-3)
+
+/* ------------------------------------------------------------------------- */
+/* Mask: which keys a query row may attend.                                   */
+/* [MAK] "Kernel structure": causal attention keeps keys up to the diagonal;   */
+/* local attention limits how far left a row may look.                         */
+/* ------------------------------------------------------------------------- */
+static int key_allowed(long i, long j, long Nq, long Nk, int causal, int window)
+{
+    long diag = i + (Nk - Nq);
+    if (j < 0 || j >= Nk) return 0;
+    if (causal && j > diag) return 0;
+    if (window >= 0 && j < diag - (long)window) return 0;
+    return 1;
+}
+
+static double dot(const double* a, const double* b, int d)
+{
+    double s = 0.0;
+    for (int t = 0; t < d; ++t) s += a[t] * b[t];
+    return s;
+}
+
+static int check_dims(int B, int Hq, int Hkv, int Nq, int Nk, int d)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0) return ORACLE_EINVAL;
+    if (Hq % Hkv != 0) return ORACLE_EINVAL;
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* One query row, materialised.                                                */
+/* [MAK] "Standard attention materializes quadratic state": S = Q K^T / sqrt d, */
+/*   P = softmax(S), O = P V  (here with an explicit scale argument).          */
+/* [AK] safe softmax: m = max(x), l = sum exp(x - m), y = exp(x - m) / l.       */
+/* The whole score row s[] and probability row p[] are formed before O.        */
+/* ------------------------------------------------------------------------- */
+static void attend_row_materialised(const double* qi, const double* kh, const double* vh,
+                                    long i, long Nq, long Nk, int d, double scale,
+                                    int causal, int window,
+                                    double* s, double* p, double* oi, double* lse_i)
+{
+    /* scores S_ij (masked entries are -inf) */
+    double m = -INFINITY;
+    for (long j = 0; j < Nk; ++j) {
+        if (key_allowed(i, j, Nq, Nk, causal, window))
+            s[j] = scale * dot(qi, kh + j * d, d);
+        else
+            s[j] = -INFINITY;
+        if (s[j] > m) m = s[j];
+    }
+    for (int t = 0; t < d; ++t) oi[t] = 0.0;
+    if (m == -INFINITY) {            /* empty row */
+        *lse_i = -INFINITY;
+        return;
+    }
+    /* safe softmax: subtract the row max, exponentiate, divide by the sum */
+    double l = 0.0;
+    for (long j = 0; j < Nk; ++j) {
+        p[j] = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - m);
+        l += p[j];
+    }
+    for (long j = 0; j < Nk; ++j) p[j] /= l;
+    /* O = P V */
+    for (long j = 0; j < Nk; ++j) {
+        if (p[j] == 0.0) continue;
+        const double* vj = vh + j * d;
+        for (int t = 0; t < d; ++t) oi[t] += p[j] * vj[t];
+    }
+    *lse_i = m + log(l);
+}
+
+/* Materialised attention for a list of (b, hq, i) rows.
+ * rows: int64 [nrows][3]; o_rows: [nrows][d]; lse_rows: [nrows]. */
+int oracle_attn_fwd_rows(const double* q, const double* k, const double* v,
+                         int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                         double scale, int causal, int window,
+                         const int64_t* rows, int64_t nrows,
+                         double* o_rows, double* lse_rows)
+{
+    if (check_dims(B, Hq, Hkv, Nq, Nk, d)) return ORACLE_EINVAL;
+    int G = Hq / Hkv;
+    for (int64_t r = 0; r < nrows; ++r) {
+        if (rows[3 * r] < 0 || rows[3 * r] >= B || rows[3 * r + 1] < 0 || rows[3 * r + 1] >= Hq ||
+            rows[3 * r + 2] < 0 || rows[3 * r + 2] >= Nq)
+            return ORACLE_EINVAL;
+    }
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        if (!s || !p) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t r = 0; r < nrows; ++r) {
+                long b = (long)rows[3 * r], h = (long)rows[3 * r + 1], i = (long)rows[3 * r + 2];
+                long hk = h / G;  /* contiguous query-head groups share one kv head */
+                const double* qi = q + (((b * Hq + h) * (long)Nq + i) * d);
+                const double* kh = k + ((b * Hkv + hk) * (long)Nk * d);
+                const double* vh = v + ((b * Hkv + hk) * (long)Nk * d);
+                attend_row_materialised(qi, kh, vh, i, Nq, Nk, d, scale, causal, window,
+                                        s, p, o_rows + r * d, lse_rows + r);
+            }
+        }
+        free(s);
+        free(p);
+    }
+    return err;
+}
+
+/* Materialised attention over every row. */
+int oracle_attn_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                    double scale, int causal, int window)
+{
+    if (check_dims(B, Hq, Hkv, Nq, Nk, d)) return ORACLE_EINVAL;
+    int64_t nrows = (int64_t)B * Hq * Nq;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * 3 * (size_t)(nrows > 0 ? nrows : 1));
+    if (!rows) return ORACLE_ENOMEM;
+    int64_t r = 0;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h)
+            for (int i = 0; i < Nq; ++i) {
+                rows[3 * r] = b; rows[3 * r + 1] = h; rows[3 * r + 2] = i; ++r;
+            }
+    int rc = oracle_attn_fwd_rows(q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, window,
+                                  rows, nrows, o, lse);
+    free(rows);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Blocked online-softmax variant.                                             */
+/* [IOA] code listing (blocked online-softmax function): the query block is    */
+/*   the outer loop; for every key/value block the running max m, running sum  */
+/*   l and running output o are corrected by exp(m - m_new) and extended.      */
+/* [MAK] "Online softmax makes tiling exact": m' = max(m, m_b),                */
+/*   l' = e^{m-m'} l + sum_j e^{s_j - m'},  o' = e^{m-m'} o + sum_j e^{s_j-m'} v_j, */
+/*   and after the final tile the output is o / l.                             */
+/* Reading for the -inf start state: while nothing has been seen (m = -inf)    */
+/*   the correction factor is 0, not e^{-inf - (-inf)}.                        */
+/* ------------------------------------------------------------------------- */
+int oracle_attn_fwd_blocked(const double* q, const double* k, const double* v, double* o, double* lse,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                            double scale, int causal, int window, int block_r, int block_c)
+{
+    if (check_dims(B, Hq, Hkv, Nq, Nk, d) || block_r <= 0 || block_c <= 0) return ORACLE_EINVAL;
+    int G = Hq / Hkv;
+    long n_rblocks = (Nq + block_r - 1) / block_r;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* m = (double*)malloc(sizeof(double) * (size_t)block_r);
+        double* l = (double*)malloc(sizeof(double) * (size_t)block_r);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)block_r * d);
+        double* s = (double*)malloc(sizeof(double) * (size_t)block_c);
+        if (!m || !l || !acc || !s) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 1) collapse(2)
+            for (long bh = 0; bh < (long)B * Hq; ++bh) {
+                for (long rb = 0; rb < n_rblocks; ++rb) {
+                    long b = bh / Hq, h = bh % Hq, hk = h / G;
+                    const double* kh = k + ((b * Hkv + hk) * (long)Nk * d);
+                    const double* vh = v + ((b * Hkv + hk) * (long)Nk * d);
+                    long i0 = rb * block_r;
+                    long i1 = i0 + block_r < Nq ? i0 + block_r : Nq;
+                    /* initialise the running state of this query block */
+                    for (long i = i0; i < i1; ++i) {
+                        m[i - i0] = -INFINITY;
+                        l[i - i0] = 0.0;
+                        for (int t = 0; t < d; ++t) acc[(i - i0) * d + t] = 0.0;
+                    }
+                    /* sweep the key/value blocks */
+                    for (long j0 = 0; j0 < Nk; j0 += block_c) {
+                        long j1 = j0 + block_c < Nk ? j0 + block_c : Nk;
+                        for (long i = i0; i < i1; ++i) {
+                            const double* qi = q + (((b * Hq + h) * (long)Nq + i) * d);
+                            double* oi = acc + (i - i0) * d;
+                            double m_b = -INFINITY;
+                            for (long j = j0; j < j1; ++j) {
+                                s[j - j0] = key_allowed(i, j, Nq, Nk, causal, window)
+                                                ? scale * dot(qi, kh + j * d, d) : -INFINITY;
+                                if (s[j - j0] > m_b) m_b = s[j - j0];
+                            }
+                            double m_old = m[i - i0];
+                            double m_new = m_b > m_old ? m_b : m_old;
+                            if (m_new == -INFINITY) continue;   /* nothing allowed so far */
+                            double corr = (m_old == -INFINITY) ? 0.0 : exp(m_old - m_new);
+                            double lsum = 0.0;
+                            for (int t = 0; t < d; ++t) oi[t] *= corr;
+                            for (long j = j0; j < j1; ++j) {
+                                if (s[j - j0] == -INFINITY) continue;
+                                double pj = exp(s[j - j0] - m_new);
+                                lsum += pj;
+                                const double* vj = vh + j * d;
+                                for (int t = 0; t < d; ++t) oi[t] += pj * vj[t];
+                            }
+                            l[i - i0] = corr * l[i - i0] + lsum;
+                            m[i - i0] = m_new;
+                        }
+                    }
+                    /* deferred normalisation: divide by l once, after the last tile */
+                    for (long i = i0; i < i1; ++i) {
+                        double* oo = o + (((b * Hq + h) * (long)Nq + i) * d);
+                        double li = l[i - i0];
+                        for (int t = 0; t < d; ++t) oo[t] = li > 0.0 ? acc[(i - i0) * d + t] / li : 0.0;
+                        lse[(b * Hq + h) * (long)Nq + i] = li > 0.0 ? m[i - i0] + log(li) : -INFINITY;
+                    }
+                }
+            }
+        }
+        free(m); free(l); free(acc); free(s);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Split-KV variant with the two-partial merge.                                */
+/* [AK] FlashDecoding: the keys of a row are cut into chunks; each chunk gives */
+/*   a partial output O_c with its own max m_c and sum l_c; the partials are   */
+/*   merged with the same rescaling:                                           */
+/*     m = max_c m_c,  l = sum_c l_c e^{m_c - m},                              */
+/*     O = sum_c O_c (l_c e^{m_c - m} / l).                                    */
+/* Each chunk is a materialised safe softmax over its own keys.                */
+/* ------------------------------------------------------------------------- */
+int oracle_attn_fwd_split(const double* q, const double* k, const double* v, double* o, double* lse,
+                          int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                          double scale, int causal, int window, int chunk)
+{
+    if (check_dims(B, Hq, Hkv, Nq, Nk, d) || chunk <= 0) return ORACLE_EINVAL;
+    int G = Hq / Hkv;
+    long n_chunks = (Nk + chunk - 1) / chunk;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* mc = (double*)malloc(sizeof(double) * (size_t)(n_chunks > 0 ? n_chunks : 1));
+        double* lc = (double*)malloc(sizeof(double) * (size_t)(n_chunks > 0 ? n_chunks : 1));
+        double* oc = (double*)malloc(sizeof(double) * (size_t)(n_chunks > 0 ? n_chunks : 1) * d);
+        double* s = (double*)malloc(sizeof(double) * (size_t)chunk);
+        if (!mc || !lc || !oc || !s) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (long row = 0; row < (long)B * Hq * Nq; ++row) {
+                long b = row / ((long)Hq * Nq), h = (row / Nq) % Hq, i = row % Nq, hk = h / G;
+                const double* qi = q + row * d;
+                const double* kh = k + ((b * Hkv + hk) * (long)Nk * d);
+                const double* vh = v + ((b * Hkv + hk) * (long)Nk * d);
+                /* one partial per chunk */
+                for (long c = 0; c < n_chunks; ++c) {
+                    long j0 = c * chunk, j1 = j0 + chunk < Nk ? j0 + chunk : Nk;
+                    double m = -INFINITY;
+                    for (long j = j0; j < j1; ++j) {
+                        s[j - j0] = key_allowed(i, j, Nq, Nk, causal, window)
+                                        ? scale * dot(qi, kh + j * d, d) : -INFINITY;
+                        if (s[j - j0] > m) m = s[j - j0];
+                    }
+                    double* o_c = oc + c * d;
+                    for (int t = 0; t < d; ++t) o_c[t] = 0.0;
+                    mc[c] = m;
+                    lc[c] = 0.0;
+                    if (m == -INFINITY) continue;
+                    for (long j = j0; j < j1; ++j) {
+                        if (s[j - j0] == -INFINITY) continue;
+                        double pj = exp(s[j - j0] - m);
+                        lc[c] += pj;
+                        for (int t = 0; t < d; ++t) o_c[t] += pj * vh[j * d + t];
+                    }
+                    for (int t = 0; t < d; ++t) o_c[t] /= lc[c];   /* normalised partial O_c */
+                }
+                /* merge */
+                double M = -INFINITY;
+                for (long c = 0; c < n_chunks; ++c) if (mc[c] > M) M = mc[c];
+                double* oo = o + row * d;
+                for (int t = 0; t < d; ++t) oo[t] = 0.0;
+                if (M == -INFINITY) { lse[row] = -INFINITY; continue; }
+                double L = 0.0;
+                for (long c = 0; c < n_chunks; ++c)
+                    if (mc[c] != -INFINITY) L += lc[c] * exp(mc[c] - M);
+                for (long c = 0; c < n_chunks; ++c) {
+                    if (mc[c] == -INFINITY) continue;
+                    double w = lc[c] * exp(mc[c] - M) / L;
+                    for (int t = 0; t < d; ++t) oo[t] += w * oc[c * d + t];
+                }
+                lse[row] = M + log(L);
+            }
+        }
+        free(mc); free(lc); free(oc); free(s);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------- */
+/* One-query decode over a paged KV cache.                                     */
+/* [MAK] "Paged attention changes addressing": for token position t of a       */
+/*   sequence, logical block = t / block_size, offset = t % block_size,        */
+/*   physical = block_table[sequence, logical block],                          */
+/*   address = cache_base + physical * block_stride + offset * token_stride.   */
+/* Cache layout [num_blocks][Hkv][block_size][d]: block_stride = Hkv*bs*d,     */
+/*   token_stride = d, and kv head h adds h*bs*d.                              */
+/* [AK] GQA: query head h reads kv head h / (Hq / Hkv).                         */
+/* The single query of sequence s attends keys 0 .. seq_lens[s]-1, materialised. */
+/* q, o: [num_seqs][Hq][d]; lse: [num_seqs][Hq].                               */
+/* ------------------------------------------------------------------------- */
+int oracle_attn_decode(const double* q, const double* k_cache, const double* v_cache,
+                       const int32_t* block_table, const int32_t* seq_lens,
+                       double* o, double* lse,
+                       int num_seqs, int Hq, int Hkv, int d, int block_size,
+                       int max_blocks_per_seq, int num_blocks, double scale)
+{
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || block_size <= 0 ||
+        max_blocks_per_seq < 0 || num_blocks < 0 || Hq % Hkv != 0)
+        return ORACLE_EINVAL;
+    for (int sq = 0; sq < num_seqs; ++sq) {
+        long L = seq_lens[sq];
+        if (L < 0 || L > (long)max_blocks_per_seq * block_size) return ORACLE_EINVAL;
+        for (long lb = 0; lb < (L + block_size - 1) / block_size; ++lb) {
+            int32_t phys = block_table[(long)sq * max_blocks_per_seq + lb];
+            if (phys < 0 || phys >= num_blocks) return ORACLE_EBOUNDS;
+        }
+    }
+    int G = Hq / Hkv;
+    long block_stride = (long)Hkv * block_size * d;
+    long token_stride = d;
+    long max_L = 0;
+    for (int sq = 0; sq < num_seqs; ++sq) if (seq_lens[sq] > max_L) max_L = seq_lens[sq];
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(max_L > 0 ? max_L : 1));
+        const double** vrow = (const double**)malloc(sizeof(double*) * (size_t)(max_L > 0 ? max_L : 1));
+        if (!s || !vrow) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 1) collapse(2)
+            for (long sq = 0; sq < num_seqs; ++sq) {
+                for (long h = 0; h < Hq; ++h) {
+                    long hk = h / G;
+                    long L = seq_lens[sq];
+                    const double* qh = q + (sq * Hq + h) * d;
+                    double m = -INFINITY;
+                    for (long t = 0; t < L; ++t) {
+                        long logical = t / block_size;
+                        long offset = t % block_size;
+                        long physical = block_table[sq * max_blocks_per_seq + logical];
+                        long addr = physical * block_stride + hk * (long)block_size * d + offset * token_stride;
+                        s[t] = scale * dot(qh, k_cache + addr, d);
+                        vrow[t] = v_cache + addr;
+                        if (s[t] > m) m = s[t];
+                    }
+                    double* oh = o + (sq * Hq + h) * d;
+                    for (int c = 0; c < d; ++c) oh[c] = 0.0;
+                    if (L == 0) { lse[sq * Hq + h] = -INFINITY; continue; }
+                    double l = 0.0;
+                    for (long t = 0; t < L; ++t) { s[t] = exp(s[t] - m); l += s[t]; }
+                    for (long t = 0; t < L; ++t) {
+                        double pt = s[t] / l;
+                        for (int c = 0; c < d; ++c) oh[c] += pt * vrow[t][c];
+                    }
+                    lse[sq * Hq + h] = m + log(l);
+                }
+            }
+        }
+        free(s);
+        free((void*)vrow);
+    }
+    return err;
+}
+
+/* Number of OpenMP threads the oracle will use (reported beside CPU timings). */
+int oracle_num_threads(void)
+{
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        {
+#ifdef _OPENMP
+            n = omp_get_num_threads();
+#endif
+        }
+    }
+    return n;
+}

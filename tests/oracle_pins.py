@@ -1,0 +1,329 @@
+"""Checks that pin the fp64 oracle to facts outside itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError on
+a mismatch. ``test_oracle_pins.py`` runs them against the committed oracle;
+``test_oracle_mutants.py`` runs them against copies with planted mistakes and
+expects at least one to fail for each mistake.
+
+What each pin rests on (pages by title and section):
+
+* blocked == materialised, split == unsplit: the tiling rule is exact
+  ("Modern attention kernels", "Online softmax makes tiling exact"; "Attention
+  kernels", safe/online softmax derivation and FlashDecoding) -- in fp64 the
+  difference is rounding only, bounded here by 1e-12.
+* probabilities sum to one (safe softmax definition) -> V = 1 gives O = 1.
+* equal scores give the mean of V; one dominant key returns its V row; the
+  first causal row sees only key 0 (closed forms).
+* translation invariance ("Flash attention and IO-aware attention", the online
+  softmax paragraph): adding a constant to a row's scores leaves O unchanged
+  and shifts lse by the constant.
+* permutation invariance of the key/value set (non-causal).
+* a window at least as long as the context equals plain causal.
+* GQA equals MHA with the kv heads duplicated ("Attention kernels", GQA).
+* paged decode equals contiguous attention for any block table ("Modern
+  attention kernels", "Paged attention changes addressing").
+* an independent numpy brute force on tiny inputs.
+* the hand-derived three-key example in ``tests/golden/three_keys.json``.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TOL = 1e-12
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _qkv(seed, B, Hq, Hkv, Nq, Nk, d):
+    r = _rng(seed)
+    return (r.standard_normal((B, Hq, Nq, d)), r.standard_normal((B, Hkv, Nk, d)),
+            r.standard_normal((B, Hkv, Nk, d)))
+
+
+def _allowed_range(i, Nq, Nk, causal, window):
+    """Allowed keys of row i as a half-open range [lo, hi) (slice form)."""
+    diag = i + (Nk - Nq)
+    hi = min(Nk, diag + 1) if causal else Nk
+    lo = max(0, diag - window) if window >= 0 else 0
+    return lo, max(lo, hi)
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a), np.asarray(b)
+    fin_a, fin_b = np.isfinite(a), np.isfinite(b)
+    assert np.array_equal(fin_a, fin_b), f"{what}: finite pattern differs"
+    assert np.array_equal(a[~fin_a], b[~fin_b]), f"{what}: non-finite values differ"
+    if fin_a.any():
+        err = np.max(np.abs(a[fin_a] - b[fin_b]))
+        assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+MASKS = [
+    # (Nq, Nk, causal, window)
+    (37, 37, False, -1),
+    (37, 37, True, -1),
+    (29, 41, True, -1),     # Nq < Nk: bottom-right causal alignment
+    (41, 29, True, -1),     # Nq > Nk: leading rows see no key
+    (40, 40, True, 5),
+    (33, 47, False, 9),     # left limit only
+    (40, 40, True, 0),      # diagonal only
+]
+
+
+def pin_blocked_equals_materialised(orc):
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        q, k, v = _qkv(100 + mi, 2, 4, 2, Nq, Nk, 8)
+        o_ref, l_ref = orc.attn_fwd(q, k, v, 0.35, causal, window)
+        for br, bc in [(1, 1), (7, 7), (16, 5), (64, 64), (Nq, Nk)]:
+            o, l = orc.attn_fwd_blocked(q, k, v, 0.35, causal, window, br, bc)
+            _close(o, o_ref, TOL, f"blocked O mask{mi} ({br},{bc})")
+            _close(l, l_ref, TOL, f"blocked lse mask{mi} ({br},{bc})")
+
+
+def pin_split_equals_unsplit(orc):
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        q, k, v = _qkv(200 + mi, 1, 4, 4, Nq, Nk, 8)
+        o_ref, l_ref = orc.attn_fwd(q, k, v, 0.4, causal, window)
+        for chunk in (1, 5, 16, Nk):
+            o, l = orc.attn_fwd_split(q, k, v, 0.4, causal, window, chunk)
+            _close(o, o_ref, TOL, f"split O mask{mi} chunk{chunk}")
+            _close(l, l_ref, TOL, f"split lse mask{mi} chunk{chunk}")
+
+
+def pin_probabilities_sum_to_one(orc):
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        q, k, _ = _qkv(300 + mi, 1, 2, 1, Nq, Nk, 6)
+        q *= 3.0
+        v = np.ones((1, 1, Nk, 6))
+        for name, (o, lse) in (("materialised", orc.attn_fwd(q, k, v, 0.5, causal, window)),
+                               ("blocked", orc.attn_fwd_blocked(q, k, v, 0.5, causal, window, 8, 8)),
+                               ("split", orc.attn_fwd_split(q, k, v, 0.5, causal, window, 7))):
+            for i in range(Nq):
+                lo, hi = _allowed_range(i, Nq, Nk, causal, window)
+                want = 1.0 if hi > lo else 0.0
+                assert np.max(np.abs(o[0, :, i, :] - want)) <= 1e-13, f"{name} row {i} mask{mi}"
+
+
+def pin_equal_scores_give_mean(orc):
+    """q = 0 makes every score 0: O is the mean of V over the allowed keys and
+    lse = ln(count). All keys equal makes every score s: lse = s + ln(count)."""
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        _, k, v = _qkv(400 + mi, 1, 2, 2, Nq, Nk, 5)
+        q0 = np.zeros((1, 2, Nq, 5))
+        o, lse = orc.attn_fwd(q0, k, v, 0.7, causal, window)
+        qr, _, _ = _qkv(450 + mi, 1, 2, 2, Nq, Nk, 5)
+        kc = np.broadcast_to(k[:, :, :1, :], k.shape).copy()
+        o2, lse2 = orc.attn_fwd(qr, kc, v, 0.7, causal, window)
+        for h in range(2):
+            for i in range(Nq):
+                lo, hi = _allowed_range(i, Nq, Nk, causal, window)
+                if hi == lo:
+                    assert np.all(o[0, h, i] == 0) and lse[0, h, i] == -np.inf
+                    continue
+                mean = v[0, h, lo:hi].mean(axis=0)
+                assert np.max(np.abs(o[0, h, i] - mean)) <= 1e-13
+                assert abs(lse[0, h, i] - math.log(hi - lo)) <= 1e-13
+                s = 0.7 * float(qr[0, h, i] @ k[0, h, 0])
+                assert np.max(np.abs(o2[0, h, i] - mean)) <= 1e-13
+                assert abs(lse2[0, h, i] - (s + math.log(hi - lo))) <= 1e-12
+
+
+def pin_dominant_key(orc):
+    """k_j* = c q with a >= 60-nat margin: O = V[j*], lse = s* to rounding."""
+    r = _rng(500)
+    d, Nk = 16, 50
+    q = r.standard_normal((1, 1, 1, d))
+    k = r.standard_normal((1, 1, Nk, d))
+    v = r.standard_normal((1, 1, Nk, d))
+    jstar = 31
+    scale = 0.25
+    others = scale * (k[0, 0] @ q[0, 0, 0])
+    c = (np.max(others) + 60.0) / (scale * float(q[0, 0, 0] @ q[0, 0, 0])) + 1.0
+    k[0, 0, jstar] = c * q[0, 0, 0]
+    sstar = scale * float(q[0, 0, 0] @ k[0, 0, jstar])
+    for fn in (lambda: orc.attn_fwd(q, k, v, scale),
+               lambda: orc.attn_fwd_blocked(q, k, v, scale, block_r=1, block_c=8),
+               lambda: orc.attn_fwd_split(q, k, v, scale, chunk=9)):
+        o, lse = fn()
+        assert np.max(np.abs(o[0, 0, 0] - v[0, 0, jstar])) <= 1e-13 * np.max(np.abs(v))
+        assert abs(lse[0, 0, 0] - sstar) <= 1e-13 * abs(sstar)
+
+
+def pin_first_causal_row(orc):
+    """With Nq == Nk and causal masking, row 0 sees key 0 only."""
+    q, k, v = _qkv(600, 2, 4, 2, 23, 23, 8)
+    o, lse = orc.attn_fwd(q, k, v, 0.3, causal=True)
+    for b in range(2):
+        for h in range(4):
+            hk = h // 2
+            assert np.max(np.abs(o[b, h, 0] - v[b, hk, 0])) <= 1e-15
+            assert abs(lse[b, h, 0] - 0.3 * float(q[b, h, 0] @ k[b, hk, 0])) <= 1e-14
+
+
+def pin_translation_invariance(orc):
+    """An extra dimension with q = 1 and k = c adds scale*c to every score."""
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        q, k, v = _qkv(700 + mi, 1, 2, 1, Nq, Nk, 6)
+        c = 3.75
+        qa = np.concatenate([q, np.ones(q.shape[:-1] + (1,))], axis=-1)
+        ka = np.concatenate([k, np.full(k.shape[:-1] + (1,), c)], axis=-1)
+        va = np.concatenate([v, np.zeros(v.shape[:-1] + (1,))], axis=-1)
+        o, lse = orc.attn_fwd(q, k, v, 0.5, causal, window)
+        oa, lsea = orc.attn_fwd(qa, ka, va, 0.5, causal, window)
+        _close(oa[..., :6], o, 1e-13, f"translated O mask{mi}")
+        fin = np.isfinite(lse)
+        assert np.array_equal(fin, np.isfinite(lsea))
+        assert np.max(np.abs(lsea[fin] - (lse[fin] + 0.5 * c))) <= 1e-12
+
+
+def pin_permutation_invariance(orc):
+    q, k, v = _qkv(800, 1, 3, 3, 19, 31, 8)
+    perm = _rng(801).permutation(31)
+    o, lse = orc.attn_fwd(q, k, v, 0.3)
+    o2, lse2 = orc.attn_fwd(q, k[:, :, perm], v[:, :, perm], 0.3)
+    _close(o2, o, 1e-13, "permuted O")
+    _close(lse2, lse, 1e-13, "permuted lse")
+
+
+def pin_long_window_is_plain_mask(orc):
+    q, k, v = _qkv(900, 1, 2, 2, 30, 30, 8)
+    oc, lc = orc.attn_fwd(q, k, v, 0.3, causal=True)
+    ow, lw = orc.attn_fwd(q, k, v, 0.3, causal=True, window=30)
+    _close(ow, oc, 0.0, "window>=Nk O")
+    _close(lw, lc, 0.0, "window>=Nk lse")
+    on, ln_ = orc.attn_fwd(q, k, v, 0.3, causal=False)
+    ow2, lw2 = orc.attn_fwd(q, k, v, 0.3, causal=False, window=60)
+    _close(ow2, on, 0.0, "noncausal long window O")
+    _close(lw2, ln_, 0.0, "noncausal long window lse")
+
+
+def pin_gqa_equals_duplicated_heads(orc):
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS[:5]):
+        q, k, v = _qkv(1000 + mi, 2, 8, 2, Nq, Nk, 8)
+        o, lse = orc.attn_fwd(q, k, v, 0.3, causal, window)
+        kd, vd = np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1)
+        o2, lse2 = orc.attn_fwd(q, kd, vd, 0.3, causal, window)
+        _close(o, o2, 0.0, f"GQA O mask{mi}")
+        _close(lse, lse2, 0.0, f"GQA lse mask{mi}")
+
+
+def _gather_contiguous(kc, vc, table, lens, s, bs):
+    L = int(lens[s])
+    tok = np.arange(L)
+    phys = table[s, tok // bs]
+    off = tok % bs
+    return kc[phys, :, off, :].transpose(1, 0, 2), vc[phys, :, off, :].transpose(1, 0, 2)
+
+
+def pin_paged_decode_equals_contiguous(orc):
+    r = _rng(1100)
+    S, Hq, Hkv, d, bs = 5, 8, 2, 8, 4
+    lens = np.array([1, 4, 5, 13, 0], dtype=np.int32)
+    nblk = (lens + bs - 1) // bs
+    nb = int(nblk.sum()) + 3
+    for identity in (True, False):
+        perm = np.arange(nb) if identity else r.permutation(nb)
+        table = np.full((S, 5), -1, dtype=np.int32)
+        pos = 0
+        for s in range(S):
+            table[s, :nblk[s]] = perm[pos:pos + nblk[s]]
+            pos += nblk[s]
+        kc = r.standard_normal((nb, Hkv, bs, d))
+        vc = r.standard_normal((nb, Hkv, bs, d))
+        q = r.standard_normal((S, Hq, d))
+        o, lse = orc.attn_decode(q, kc, vc, table, lens, 0.4)
+        for s in range(S):
+            ks, vs = _gather_contiguous(kc, vc, table, lens, s, bs)
+            if lens[s] == 0:
+                assert np.all(o[s] == 0) and np.all(lse[s] == -np.inf)
+                continue
+            of, lf = orc.attn_fwd(q[s][None, :, None, :], ks[None], vs[None], 0.4)
+            _close(o[s], of[0, :, 0, :], 1e-14, f"decode O seq{s}")
+            _close(lse[s], lf[0, :, 0], 1e-14, f"decode lse seq{s}")
+
+
+def pin_numpy_bruteforce(orc):
+    """Independent vectorised restatement on tiny inputs."""
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        q, k, v = _qkv(1200 + mi, 2, 4, 2, Nq, Nk, 3)
+        o, lse = orc.attn_fwd(q, k, v, 0.6, causal, window)
+        kk = np.repeat(k, 2, axis=1)
+        vv = np.repeat(v, 2, axis=1)
+        s = 0.6 * np.einsum("bhid,bhjd->bhij", q, kk)
+        i = np.arange(Nq)[:, None]
+        j = np.arange(Nk)[None, :]
+        diag = i + (Nk - Nq)
+        keep = np.ones((Nq, Nk), dtype=bool)
+        if causal:
+            keep &= j <= diag
+        if window >= 0:
+            keep &= j >= diag - window
+        s = np.where(keep, s, -np.inf)
+        with np.errstate(invalid="ignore", divide="ignore"):
+            lse_np = np.log(np.sum(np.exp(s), axis=-1))
+            p = np.exp(s - lse_np[..., None])
+        p = np.nan_to_num(p, nan=0.0)
+        o_np = np.einsum("bhij,bhjd->bhid", p, vv)
+        _close(o, o_np, 1e-12, f"numpy O mask{mi}")
+        _close(lse, lse_np, 1e-12, f"numpy lse mask{mi}")
+
+
+def pin_golden_three_keys(orc):
+    with open(os.path.join(GOLDEN, "three_keys.json")) as f:
+        g = json.load(f)
+    q = np.array(g["q"], dtype=np.float64)[None, None, None, :]
+    k = np.array(g["k"], dtype=np.float64)[None, None]
+    v = np.array(g["v"], dtype=np.float64)[None, None]
+    for fn in (lambda: orc.attn_fwd(q, k, v, g["scale"]),
+               lambda: orc.attn_fwd_blocked(q, k, v, g["scale"], block_r=1, block_c=2),
+               lambda: orc.attn_fwd_split(q, k, v, g["scale"], chunk=2)):
+        o, lse = fn()
+        assert np.max(np.abs(o[0, 0, 0] - np.array(g["o"]))) <= 1e-14
+        assert abs(lse[0, 0, 0] - g["lse"]) <= 1e-14
+
+
+def pin_large_logits_and_late_maximum(orc):
+    """Scores rising along the keys (largest last) and logits near 700, where a
+    softmax without the max subtraction overflows."""
+    d, Nk = 4, 64
+    q = np.zeros((1, 1, 1, d))
+    q[0, 0, 0, 0] = 1.0
+    k = np.zeros((1, 1, Nk, d))
+    k[0, 0, :, 0] = np.linspace(0.0, 700.0, Nk)  # strictly increasing scores
+    v = _rng(1300).standard_normal((1, 1, Nk, d))
+    o, lse = orc.attn_fwd(q, k, v, 1.0)
+    assert np.all(np.isfinite(o)) and np.isfinite(lse).all()
+    gap = 700.0 / (Nk - 1)
+    w = np.exp(-gap * np.arange(Nk)[::-1])        # relative weights to the last key
+    want = (w[:, None] * v[0, 0]).sum(0) / w.sum()
+    assert np.max(np.abs(o[0, 0, 0] - want)) <= 1e-13
+    assert abs(lse[0, 0, 0] - (700.0 + math.log(w.sum()))) <= 1e-12
+    for bc in (1, 3, 16):
+        ob, lb = orc.attn_fwd_blocked(q, k, v, 1.0, block_r=1, block_c=bc)
+        _close(ob, o, 1e-13, f"late-max blocked bc={bc}")
+        _close(lb, lse, 1e-12, f"late-max blocked lse bc={bc}")
+
+
+ALL_PINS = [
+    pin_blocked_equals_materialised,
+    pin_split_equals_unsplit,
+    pin_probabilities_sum_to_one,
+    pin_equal_scores_give_mean,
+    pin_dominant_key,
+    pin_first_causal_row,
+    pin_translation_invariance,
+    pin_permutation_invariance,
+    pin_long_window_is_plain_mask,
+    pin_gqa_equals_duplicated_heads,
+    pin_paged_decode_equals_contiguous,
+    pin_numpy_bruteforce,
+    pin_golden_three_keys,
+    pin_large_logits_and_late_maximum,
+]
