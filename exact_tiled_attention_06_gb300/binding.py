@@ -1,0 +1,171 @@
+"""Thin ctypes binding over libattn.so (include/attn.h), same names as the C ABI.
+
+Only argument marshalling happens here: torch tensors provide device memory and
+the current CUDA stream; every step of the computation runs in the library's
+kernels. There is no fallback: if the library is missing or returns an error,
+these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import buildlib as _build
+
+ATTN_OK = 0
+STATUS_NAMES = {
+    0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED", -3: "ATTN_ERR_MISALIGNED",
+    -4: "ATTN_ERR_WORKSPACE", -5: "ATTN_ERR_LAUNCH", -6: "ATTN_ERR_DEVICE_TIMEOUT", -7: "ATTN_ERR_DEVICE_BOUNDS",
+    -8: "ATTN_ERR_CUDA",
+}
+
+# Every symbol include/attn.h declares.
+EXPORTED = ("attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_decode_chunk_tokens",
+            "attn_get_device_error", "attn_kv_layout_version", "attn_status_string")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where} failed: {STATUS_NAMES.get(status, status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libattn.so (it must have been built with ``build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"libattn.so is not built ({p}); run exact_tiled_attention_06_gb300.build()")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+        lib.attn_fwd.restype = i
+        lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+        lib.attn_decode_workspace_size.restype = sz
+        lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, vp]
+        lib.attn_decode.restype = i
+        lib.attn_decode_chunk_tokens.argtypes = [i, i, i, i]
+        lib.attn_decode_chunk_tokens.restype = i
+        lib.attn_get_device_error.argtypes = [vp]
+        lib.attn_get_device_error.restype = i
+        lib.attn_kv_layout_version.argtypes = []
+        lib.attn_kv_layout_version.restype = i
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_kv_layout_version() -> int:
+    return int(load_library().attn_kv_layout_version())
+
+
+def attn_get_device_error(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device error word."""
+    return int(load_library().attn_get_device_error(_stream_handle(stream)))
+
+
+def attn_fwd(q, k, v, causal=False, window=-1, scale=None, out=None, lse=None, stream=None):
+    """Prefill attention. q [B][Hq][Nq][d], k/v [B][Hkv][Nk][d] bf16 (CUDA, contiguous).
+    Returns (o bf16 [B][Hq][Nq][d], lse fp32 [B][Hq][Nq])."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if Bk != B or dk != d or v.shape != k.shape:
+        raise ValueError("q/k/v shapes disagree")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                 float(scale), int(bool(causal)), int(window), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_decode_workspace_size(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_seq) -> int:
+    return int(load_library().attn_decode_workspace_size(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_seq))
+
+
+def attn_decode_chunk_tokens(num_seqs, Hkv, block_size, max_blocks_per_seq) -> int:
+    return int(load_library().attn_decode_chunk_tokens(num_seqs, Hkv, block_size, max_blocks_per_seq))
+
+
+def attn_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, workspace=None, out=None, lse=None,
+                stream=None):
+    """Paged one-query decode. q [S][Hq][d] bf16; caches [num_blocks][Hkv][bs][d] bf16;
+    block_table int32 [S][max_blocks]; seq_lens int32 [S]. Returns (o [S][Hq][d], lse [S][Hq])."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    S, Hq, d = q.shape
+    nb, Hkv, bs, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape or block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("decode shapes disagree")
+    mb = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+                                    _ptr(out), _ptr(lse), S, Hq, Hkv, d, bs, mb, nb, float(scale),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode")
+    return out, lse

@@ -1,0 +1,564 @@
+// fwd_kernel.cu -- prefill attention for sm_103a.
+//
+// One CTA owns two 128-row query tiles that read the same K/V stream (two query
+// heads of one kv head when the GQA group is even, else two consecutive row tiles
+// of one head). Roles, by warp:
+//   warps 0-3  softmax for query tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    tcgen05 MMA issue (one thread) and TMEM allocation
+//   warp  9    TMA producer (one thread): Q tiles, then the K/V ring
+//
+// Per key tile j and query tile t (pages: "Modern attention kernels", sections
+// "Online softmax makes tiling exact" and "Kernel structure"; "Attention kernels",
+// the FlashAttention-2/3 paragraphs on query-outer order, warp specialisation and
+// asynchronous copies):
+//   S_t = Q_t K_j^T           tcgen05.mma, bf16 x bf16 -> fp32 in TMEM (128 x 128)
+//   softmax warps             m' = max(m, rowmax), p = 2^(s*scale*log2e - m'),
+//                             l = alpha*l + sum p, P (bf16) written back over S_t
+//   O_t = alpha*O_t + P_t V_j tcgen05.mma with P from TMEM, V from shared memory
+// and after the last tile O/l (bf16) and lse = ln2 * (m + log2 l) are written.
+// The running max is only moved when a row's max rises by more than 2^8 (lazy
+// rescale); the result is unchanged because l and O always share the same max.
+//
+// Key tiles wholly outside the causal/window band are never visited; the tiles that
+// cross the band edge or the end of the keys are masked per element.
+#include <climits>
+#include <cmath>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;  // keys per tile
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kFwdThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: move the max only if it rises by > 256x
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kBoxes = D / 64;            // 128-byte-wide TMA boxes per row
+    static constexpr int kBoxBytes = 128 * 128;      // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;
+    static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots (K and V alternate)
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kNumBars = 1 + 2 * kStages + 7;
+    static constexpr int kHolderOff = kBarOff + 8 * kNumBars;
+    static constexpr int kAbortOff = kHolderOff + 4;
+    static constexpr int kUsedBytes = kAbortOff + 4;
+    static constexpr int kSmemBytes = kUsedBytes + 1024;  // slack for the 1024-byte alignment
+    static constexpr uint32_t kTmemCols = 512;            // S0 | S1 | O0 | O1
+    static constexpr uint32_t kOCol = 2 * BN;
+    static_assert(kUsedBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kOCol + 2 * D <= kTmemCols, "TMEM budget");
+};
+
+struct FwdParams {
+    __nv_bfloat16* o;
+    float* lse;
+    int B, Hq, Hkv, Nq, Nk, G;
+    float scale_log2;  // scale * log2(e)
+    int causal, window;
+    int pair_heads;    // 1: tiles are query heads (2u, 2u+1) at one row tile; 0: row tiles (2r, 2r+1)
+    int n_row_units;   // row units per (batch, head unit)
+    int n_hunits;      // head units per batch entry
+    unsigned* err;
+};
+
+struct TileWork {
+    int head;   // query head
+    int row0;   // first query row
+    int rows;   // valid rows in the tile (0: no tile)
+    int kv_lo;  // first key tile visited
+    int kv_hi;  // one past the last key tile visited
+};
+
+// Key tiles a query tile must visit: causal keeps keys j <= i + (Nk - Nq); a window
+// w >= 0 also needs j >= i + (Nk - Nq) - w.
+__device__ __forceinline__ TileWork make_tile(const FwdParams& p, int head, int row0)
+{
+    TileWork t{head, row0, 0, 0, 0};
+    int rows = p.Nq - row0;
+    if (rows > BM) rows = BM;
+    if (rows <= 0) return t;
+    t.rows = rows;
+    const long long delta = static_cast<long long>(p.Nk) - p.Nq;
+    long long key_hi = p.Nk;
+    if (p.causal) {
+        const long long h = static_cast<long long>(row0) + rows + delta;
+        if (h < key_hi) key_hi = h;
+    }
+    long long key_lo = 0;
+    if (p.window >= 0) {
+        const long long l = static_cast<long long>(row0) + delta - p.window;
+        if (l > key_lo) key_lo = l;
+    }
+    if (key_hi > key_lo) {
+        t.kv_lo = static_cast<int>(key_lo / BN);
+        t.kv_hi = static_cast<int>((key_hi + BN - 1) / BN);
+    }
+    return t;
+}
+
+// True when every key of tile j is allowed for every valid row of the query tile.
+__device__ __forceinline__ bool tile_unmasked(const FwdParams& p, const TileWork& t, int j)
+{
+    const long long k0 = static_cast<long long>(j) * BN, k1 = k0 + BN;
+    const long long delta = static_cast<long long>(p.Nk) - p.Nq;
+    if (k1 > p.Nk) return false;
+    if (p.causal && k1 - 1 > t.row0 + delta) return false;
+    if (p.window >= 0 && k0 < static_cast<long long>(t.row0) + t.rows - 1 + delta - p.window) return false;
+    return true;
+}
+
+__device__ __forceinline__ bool tile_active(const TileWork& t, int j)
+{
+    return t.rows > 0 && t.kv_lo <= j && j < t.kv_hi;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
+{
+    using C = FwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work unit (heaviest row units first, which balances the causal triangle)
+    const int n_bh = p.B * p.n_hunits;
+    const int unit = blockIdx.x;
+    const int ru = p.n_row_units - 1 - unit / n_bh;
+    const int bh = unit % n_bh;
+    const int b = bh / p.n_hunits;
+    const int hu = bh % p.n_hunits;
+    TileWork tw[2];
+    if (p.pair_heads) {
+        tw[0] = make_tile(p, 2 * hu, ru * BM);
+        tw[1] = make_tile(p, 2 * hu + 1, ru * BM);
+    } else {
+        tw[0] = make_tile(p, hu, 2 * ru * BM);
+        tw[1] = make_tile(p, hu, (2 * ru + 1) * BM);
+    }
+    const int hkv = tw[0].head / p.G;
+    const bool act[2] = {tw[0].rows > 0 && tw[0].kv_lo < tw[0].kv_hi, tw[1].rows > 0 && tw[1].kv_lo < tw[1].kv_hi};
+    int lo = INT_MAX, hi = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (act[t]) {
+            lo = min(lo, tw[t].kv_lo);
+            hi = max(hi, tw[t].kv_hi);
+        }
+    }
+    const bool has_work = lo < hi;
+
+    // ---- barriers
+    const uint32_t bar0 = sb + C::kBarOff;
+    const uint32_t bar_q = bar0;
+    auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
+    auto s_full = [&](int t) { return bar0 + 8u * (1 + 2 * C::kStages + t); };
+    auto p_full = [&](int t) { return bar0 + 8u * (3 + 2 * C::kStages + t); };
+    auto o_done = [&](int t) { return bar0 + 8u * (5 + 2 * C::kStages + t); };
+    const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::kStages);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), 128);
+            mbar_init(o_done(t), 1);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    const uint32_t sQ = sb + C::kQOff;
+    const uint32_t sRing = sb + C::kRingOff;
+
+    if (warp == kLoadWarp) {
+        // ================================================================ producer
+        if (lane == 0 && has_work) {
+            uint32_t qbytes = 0;
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if (act[t]) qbytes += C::kTileBytes;
+            mbar_arrive_expect_tx(bar_q, qbytes);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!act[t]) continue;
+#pragma unroll
+                for (int x = 0; x < C::kBoxes; ++x)
+                    tma_load_3d(sQ + t * C::kTileBytes + x * C::kBoxBytes, &tm_q, bar_q, 64 * x, tw[t].row0,
+                                b * p.Hq + tw[t].head);
+            }
+            int n = 0;
+            bool ok = true;
+            for (int j = lo; j < hi && ok; ++j) {
+#pragma unroll
+                for (int kind = 0; kind < 2; ++kind) {
+                    const int s = n % C::kStages;
+                    if (n >= C::kStages &&
+                        !mbar_wait(kv_empty(s), ((n / C::kStages) - 1) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(kv_full(s), C::kTileBytes);
+                    const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+#pragma unroll
+                    for (int x = 0; x < C::kBoxes; ++x)
+                        tma_load_3d(sRing + s * C::kTileBytes + x * C::kBoxBytes, map, kv_full(s), 64 * x, j * BN,
+                                    b * p.Hkv + hkv);
+                    ++n;
+                }
+            }
+            // Never leave while a copy into this block's shared memory is in flight.
+            mbar_wait(bar_q, 0, nullptr, p.err);
+            for (int s = 0; s < C::kStages; ++s) {
+                const int fills = n / C::kStages + (s < n % C::kStages ? 1 : 0);
+                if (fills > 0) mbar_wait(kv_full(s), (fills - 1) & 1, nullptr, p.err);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================================================ MMA issue
+        if (lane == 0 && has_work) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+            // S_t = Q_t K^T: both operands K-major; a 16-wide k step is 32 bytes inside a
+            // 128-byte swizzle row, and every 64 columns start a new box.
+            auto issue_qk = [&](int t, int slot) {
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * BN);
+                const uint32_t a0 = sQ + t * C::kTileBytes;
+                const uint32_t b0 = sRing + slot * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+                    mma_ss(d_tmem, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024),
+                           idesc_qk, kk > 0 ? 1u : 0u);
+                }
+            };
+            // O_t (+)= P_t V: P from TMEM (8 columns = 16 bf16 keys per step); V is
+            // MN-major in shared memory: 16 keys = 2048 bytes per step, the two
+            // 64-column halves of d are one box (kBoxBytes) apart.
+            auto issue_pv = [&](int t, int slot, bool accumulate) {
+                const uint32_t d_tmem = tmem + C::kOCol + static_cast<uint32_t>(t * D);
+                const uint32_t a_tmem = tmem + static_cast<uint32_t>(t * BN);
+                const uint32_t v0 = sRing + slot * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(v0 + kk * 2048, C::kBoxBytes, 1024), idesc_pv,
+                           (accumulate || kk > 0) ? 1u : 0u);
+            };
+
+            bool ok = mbar_wait(bar_q, 0, abort_flag, p.err);
+            tc_fence_after();
+            int n = 0;
+            uint32_t pphase[2] = {0u, 0u};
+            bool first_pv[2] = {true, true};
+            if (ok) {
+                const int ks = n % C::kStages;
+                ok = mbar_wait(kv_full(ks), (n / C::kStages) & 1, abort_flag, p.err);
+                tc_fence_after();
+                ++n;
+                if (ok) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (tile_active(tw[t], lo)) {
+                            issue_qk(t, ks);
+                            tc_commit(s_full(t));
+                        }
+                    tc_commit(kv_empty(ks));
+                }
+            }
+            for (int j = lo; j < hi && ok; ++j) {
+                const int vs = n % C::kStages;
+                if (!mbar_wait(kv_full(vs), (n / C::kStages) & 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                ++n;
+                const bool has_next = j + 1 < hi;
+                const int ks = n % C::kStages;
+                // tile 0: O0 += P0 V_j, then S0 for the next key tile
+                if (tile_active(tw[0], j)) {
+                    if (!mbar_wait(p_full(0), pphase[0], abort_flag, p.err)) break;
+                    pphase[0] ^= 1u;
+                    tc_fence_after();
+                    issue_pv(0, vs, !first_pv[0]);
+                    first_pv[0] = false;
+                    if (j == tw[0].kv_hi - 1) tc_commit(o_done(0));
+                }
+                if (has_next) {
+                    if (!mbar_wait(kv_full(ks), (n / C::kStages) & 1, abort_flag, p.err)) break;
+                    tc_fence_after();
+                    ++n;
+                    if (tile_active(tw[0], j + 1)) {
+                        issue_qk(0, ks);
+                        tc_commit(s_full(0));
+                    }
+                }
+                // tile 1: O1 += P1 V_j, then S1 for the next key tile
+                if (tile_active(tw[1], j)) {
+                    if (!mbar_wait(p_full(1), pphase[1], abort_flag, p.err)) break;
+                    pphase[1] ^= 1u;
+                    tc_fence_after();
+                    issue_pv(1, vs, !first_pv[1]);
+                    first_pv[1] = false;
+                    if (j == tw[1].kv_hi - 1) tc_commit(o_done(1));
+                }
+                tc_commit(kv_empty(vs));
+                if (has_next) {
+                    if (tile_active(tw[1], j + 1)) {
+                        issue_qk(1, ks);
+                        tc_commit(s_full(1));
+                    }
+                    tc_commit(kv_empty(ks));
+                }
+            }
+            // Never release TMEM while an MMA may still be running.
+            tc_commit(bar_drain);
+            mbar_wait(bar_drain, 0, nullptr, p.err);
+        }
+    } else {
+        // ================================================================ softmax (warps 0-7)
+        const int t = warp >> 2;
+        const int quarter = warp & 3;
+        const TileWork T = t ? tw[1] : tw[0];
+        const int r = quarter * 32 + lane;  // row in the tile = TMEM lane
+        const int row = T.row0 + r;
+        const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_sel + static_cast<uint32_t>(t * BN);
+        const uint32_t o_tmem = tmem + lane_sel + C::kOCol + static_cast<uint32_t>(t * D);
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY;  // running max, scaled log2 units
+        float l = 0.0f;       // running sum
+        int n_act = 0;
+        bool ok = true;
+        const bool tile_has = t ? act[1] : act[0];
+        if (tile_has) {
+            const long long diag = static_cast<long long>(row) + (static_cast<long long>(p.Nk) - p.Nq);
+            long long key_max = static_cast<long long>(p.Nk) - 1;
+            if (p.causal && diag < key_max) key_max = diag;
+            const long long key_min = p.window >= 0 ? diag - p.window : LLONG_MIN / 4;
+            for (int j = T.kv_lo; j < T.kv_hi; ++j) {
+                if (!mbar_wait(s_full(t), n_act & 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sr[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tmem + 32 * c, sr + 32 * c);
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) tmem_ld_wait_dep32(sr + 32 * c);
+                float s[BN];
+#pragma unroll
+                for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
+                if (!tile_unmasked(p, T, j)) {
+                    const long long kbase = static_cast<long long>(j) * BN;
+                    long long hi_rel = key_max - kbase;
+                    long long lo_rel = key_min - kbase;
+                    const int hi_c = hi_rel < -1 ? -1 : (hi_rel > BN ? BN : static_cast<int>(hi_rel));
+                    const int lo_c = lo_rel < 0 ? 0 : (lo_rel > BN + 1 ? BN + 1 : static_cast<int>(lo_rel));
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (c > hi_c || c < lo_c) s[c] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < BN; c += 4) {
+                    mx0 = fmaxf(mx0, s[c]);
+                    mx1 = fmaxf(mx1, s[c + 1]);
+                    mx2 = fmaxf(mx2, s[c + 2]);
+                    mx3 = fmaxf(mx3, s[c + 3]);
+                }
+                const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const bool need = m_cand > m + kRescaleThreshold || (m == -INFINITY && m_cand > -INFINITY);
+                float alpha = 1.0f;
+                const bool rescale = __any_sync(0xffffffffu, need);
+                if (rescale) {
+                    const float m_new = fmaxf(m, m_cand);
+                    alpha = (m == -INFINITY) ? 0.0f : ex2_approx(m - m_new);
+                    m = m_new;
+                }
+                const float base = (m == -INFINITY) ? 0.0f : m;
+                float sum0 = 0.0f, sum1 = 0.0f;
+                uint32_t pk[BN / 2];
+#pragma unroll
+                for (int c = 0; c < BN; c += 2) {
+                    const float p0 = ex2_approx(fmaf(s[c], sl2, -base));
+                    const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -base));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[c / 2] = pack_bf16x2(p0, p1);
+                }
+                // P (bf16 pairs) over the first 64 columns of S_t
+                tmem_st32(s_tmem, pk);
+                tmem_st32(s_tmem + 32, pk + 32);
+                l = l * alpha + (sum0 + sum1);
+                if (rescale && n_act > 0) {
+                    // O <- alpha * O. The previous P V has finished: it was issued before
+                    // the S MMA whose completion was just observed.
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(o_tmem + 32 * c, ov);
+                        tmem_ld_wait_dep32(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(o_tmem + 32 * c, ov);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_full(t));
+                ++n_act;
+            }
+        }
+        // ---- epilogue: O / l -> bf16, lse = ln2 * (m + log2 l)
+        if (T.rows > 0 && ok) {
+            const bool valid_row = row < p.Nq;
+            const size_t row_idx = (static_cast<size_t>(b) * p.Hq + T.head) * p.Nq + row;
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            if (tile_has) {
+                if (mbar_wait(o_done(t), 0, abort_flag, p.err)) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(o_tmem + 32 * c, ov);
+                        tmem_ld_wait_dep32(ov);
+                        if (valid_row) {
+                            uint4* dst = reinterpret_cast<uint4*>(p.o + row_idx * D + 32 * c);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint4 w;
+                                w.x = pack_bf16x2(__uint_as_float(ov[8 * i + 0]) * inv_l,
+                                                  __uint_as_float(ov[8 * i + 1]) * inv_l);
+                                w.y = pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv_l,
+                                                  __uint_as_float(ov[8 * i + 3]) * inv_l);
+                                w.z = pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv_l,
+                                                  __uint_as_float(ov[8 * i + 5]) * inv_l);
+                                w.w = pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv_l,
+                                                  __uint_as_float(ov[8 * i + 7]) * inv_l);
+                                dst[i] = w;
+                            }
+                        }
+                    }
+                    if (valid_row) p.lse[row_idx] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                }
+            } else if (valid_row) {
+                // no key is allowed for any row of this tile
+                uint4* dst = reinterpret_cast<uint4*>(p.o + row_idx * D);
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+                p.lse[row_idx] = -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D>
+int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                 int Nk, float scale, int causal, int window, cudaStream_t stream, unsigned* err)
+{
+    using C = FwdCfg<D>;
+    CUtensorMap tq, tk, tv;
+    const uint32_t box[3] = {64u, 128u, 1u};
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nq),
+                                  static_cast<uint64_t>(B) * Hq};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Nq) * D * 2};
+        int rc = encode_bf16_map(&tq, q, 3, dims, strides, box);
+        if (rc != kOk) return rc;
+    }
+    if (Nk > 0) {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nk), static_cast<uint64_t>(B) * Hkv};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Nk) * D * 2};
+        int rc = encode_bf16_map(&tk, k, 3, dims, strides, box);
+        if (rc != kOk) return rc;
+        rc = encode_bf16_map(&tv, v, 3, dims, strides, box);
+        if (rc != kOk) return rc;
+    } else {
+        // No keys: no K/V tile is ever loaded, the descriptors are placeholders.
+        tk = tq;
+        tv = tq;
+    }
+    FwdParams prm;
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Nq = Nq;
+    prm.Nk = Nk;
+    prm.G = Hq / Hkv;
+    prm.scale_log2 = scale * kLog2e;
+    prm.causal = causal ? 1 : 0;
+    prm.window = window < 0 ? -1 : window;
+    prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+    const int n_row_tiles = (Nq + BM - 1) / BM;
+    prm.n_row_units = prm.pair_heads ? n_row_tiles : (n_row_tiles + 1) / 2;
+    prm.n_hunits = prm.pair_heads ? Hq / 2 : Hq;
+    prm.err = err;
+    const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
+    if (grid <= 0) return kOk;
+    if (grid > INT_MAX) return kErrInvalidArg;
+
+    if (cudaFuncSetAttribute(attn_fwd_sm103<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return kErrCuda;
+    attn_fwd_sm103<D><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+}
+
+}  // namespace
+
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+               int Nk, int d, float scale, int causal, int window, cudaStream_t stream, unsigned* err)
+{
+    if (Nq == 0) return kOk;
+    if (d == 128) return launch_fwd_d<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream, err);
+    if (d == 64) return launch_fwd_d<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream, err);
+    return kErrUnsupported;
+}
+
+}  // namespace attn

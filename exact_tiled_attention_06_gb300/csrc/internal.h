@@ -1,0 +1,57 @@
+// internal.h -- host-side declarations shared by the translation units of libattn.so.
+// Nothing here is exported; the public interface is include/attn.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Status values (same numbers as attn_status in include/attn.h).
+enum : int {
+    kOk = 0,
+    kErrInvalidArg = -1,
+    kErrUnsupported = -2,
+    kErrMisaligned = -3,
+    kErrWorkspace = -4,
+    kErrLaunch = -5,
+    kErrDeviceTimeout = -6,
+    kErrDeviceBounds = -7,
+    kErrCuda = -8,
+};
+
+// Encode a tiled TMA descriptor over a bf16 tensor with the 128-byte swizzle.
+// dims[0] is the innermost (contiguous) extent; strides_bytes[i] is the byte stride
+// of dimension i+1. Out-of-range box elements read as zero.
+int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+
+// Device address of the library's error word on the current device (nullptr on failure).
+unsigned* device_error_word();
+
+// Prefill (implemented in fwd_kernel.cu). Arguments are already validated.
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+               int Nq, int Nk, int d, float scale, int causal, int window, cudaStream_t stream,
+               unsigned* err);
+
+// Split-KV decode plan: the chunk length and the workspace carve-up.
+struct DecodePlan {
+    int chunk;          // keys per split (multiple of 16 and of block_size)
+    int n_split_max;    // splits of the longest possible sequence
+    int n_hgroups;      // groups of at most 16 query heads per kv head
+    size_t lse_offset;  // byte offset of the partial log-sums  [n_split_max][num_seqs][Hq] fp32
+    size_t o_offset;    // byte offset of the partial outputs   [n_split_max][num_seqs][Hq][d] fp32
+    size_t bytes;       // total workspace bytes
+};
+bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
+                 DecodePlan* plan);
+
+// Decode (implemented in decode_kernel.cu). Arguments are already validated.
+int launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                  const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
+                  int block_size, int max_blocks_per_seq, int num_blocks, float scale, void* workspace,
+                  const DecodePlan& plan, cudaStream_t stream, unsigned* err);
+
+}  // namespace attn

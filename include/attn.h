@@ -1,0 +1,150 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact tiled attention library (libattn.so).
+ *
+ * Exact scaled-dot-product attention computed tile by tile with the online-softmax
+ * update; the N x N score matrix never reaches device memory.
+ *
+ * Pages cited (by title and section):
+ *   "Modern attention kernels" (blog.ecitis.org)                -- MAK
+ *   "Flash attention and IO-aware attention" (aigrafen.se)      -- IOA
+ *   "Attention kernels" (inference.tusharamrit.in)              -- AK
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device, row-major
+ *    and contiguous. bf16 tensors and workspaces must be 16-byte aligned; fp32 and
+ *    int32 arrays 4-byte aligned. bf16 tensors are passed as void*.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Every launch is asynchronous on that stream; the library never synchronises it.
+ *  - The caller owns every buffer (inputs, outputs, workspace). The library never
+ *    allocates or frees device memory.
+ *  - Host-detectable problems return a negative attn_status before anything is
+ *    launched. Problems the kernels detect (a block-table entry out of range, a
+ *    pipeline wait that ran out of time) set a device error word that
+ *    attn_get_device_error() reads and clears. Kernels never trap.
+ *  - Supported head dimensions: d in {64, 128}. Device: compute capability 10.3.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1,     /* null pointer, bad size, Hq % Hkv != 0, scale <= 0 ... */
+    ATTN_ERR_UNSUPPORTED = -2,     /* d not in {64,128}, block_size not a multiple of 16, non-sm_103 device */
+    ATTN_ERR_MISALIGNED = -3,      /* a pointer is not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = -4,       /* decode workspace missing or smaller than attn_decode_workspace_size() */
+    ATTN_ERR_LAUNCH = -5,          /* a kernel launch failed */
+    ATTN_ERR_DEVICE_TIMEOUT = -6,  /* a bounded pipeline wait inside a kernel ran out of time */
+    ATTN_ERR_DEVICE_BOUNDS = -7,   /* a kernel met a block-table entry outside [0, num_blocks) */
+    ATTN_ERR_CUDA = -8             /* a CUDA runtime call made by the host side failed */
+} attn_status;
+
+/*
+ * attn_fwd -- prefill attention: O = softmax(scale * Q K^T + mask) V, plus per-row lse.
+ *
+ *   MAK "Standard attention materializes quadratic state" (S = Q K^T / sqrt(d),
+ *   P = softmax(S), O = P V); MAK "Online softmax makes tiling exact" (running max m,
+ *   running sum l, unnormalised accumulator o, rescaled by exp(m - m') and divided by
+ *   l once at the end); MAK "Kernel structure" (causal tiles above the diagonal are
+ *   skipped, the boundary tile is masked; local attention narrows the visited range);
+ *   MAK "Backward pass recomputes scores" (the per-row statistic that is saved).
+ *
+ *   q   : bf16 [B][Hq][Nq][d]          (input)
+ *   k, v: bf16 [B][Hkv][Nk][d]         (input)  query head h reads kv head h / (Hq/Hkv)
+ *   o   : bf16 [B][Hq][Nq][d]          (output) rounded to nearest even from fp32
+ *   lse : fp32 [B][Hq][Nq]             (output) natural-log sum of exp of the scaled
+ *                                       scores of the row; -inf for a row with no key
+ *   scale  : > 0, multiplies q.k (1/sqrt(d) for standard attention)
+ *   causal : nonzero -> row i sees keys j <= i + (Nk - Nq) (bottom-right alignment)
+ *   window : >= 0 -> row i also needs j >= i + (Nk - Nq) - window; < 0 -> no left limit
+ *   A row with no allowed key gets O = 0 and lse = -inf.
+ *   Sizes: B, Hq, Hkv >= 1; Nq, Nk >= 0 (0 is a no-op); every product fits in int32 rows.
+ *   Returns ATTN_OK or a negative attn_status.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+             int causal, int window, void* stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of scratch attn_decode needs for these sizes.
+ *
+ *   AK FlashDecoding: each chunk of a sequence's keys produces a partial output with
+ *   its own max and sum; the partials are merged afterwards. The workspace holds
+ *   those partials (fp32) for the largest possible split count of the batch.
+ *   Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int block_size,
+                                  int max_blocks_per_seq);
+
+/*
+ * attn_decode -- one query token per sequence against a paged KV cache.
+ *
+ *   MAK "Prefill and decode need different kernels" (coalesced cache reads, parallel
+ *   reduction across the context, grouped-query head sharing, cache block
+ *   indirection); MAK "Paged attention changes addressing" (logical block =
+ *   pos / block_size, offset = pos % block_size, physical = block_table[seq, block],
+ *   address = base + physical * block_stride + offset * token_stride);
+ *   AK FlashDecoding (split-KV partials merged with the online-softmax rescaling);
+ *   AK GQA (the query heads of one kv head read it once).
+ *
+ *   q          : bf16 [num_seqs][Hq][d]                         (input)
+ *   k_cache,
+ *   v_cache    : bf16 [num_blocks][Hkv][block_size][d]          (input, layout version 1)
+ *   block_table: int32 [num_seqs][max_blocks_per_seq]          (input) physical block of
+ *                each logical block; entries past a sequence's length are never read
+ *   seq_lens   : int32 [num_seqs]                               (input, device) keys per
+ *                sequence, 0 <= L <= max_blocks_per_seq * block_size (not read by the host)
+ *   o          : bf16 [num_seqs][Hq][d]                         (output)
+ *   lse        : fp32 [num_seqs][Hq]                            (output) -inf when L = 0
+ *   block_size : multiple of 16, at most 256.  num_seqs <= 65535 (0 is a no-op).
+ *   num_blocks * Hkv * block_size must stay below 2^31 (cache rows are addressed
+ *   with 32-bit TMA coordinates).
+ *   workspace  : device scratch of at least attn_decode_workspace_size(...) bytes,
+ *                16-byte aligned; contents need no initialisation and are clobbered.
+ *   Two calls that share a workspace must not overlap on the device.
+ *   Cache slots past a sequence's length (the tail of its last block) are never used,
+ *   whatever they hold. A block-table entry outside [0, num_blocks) sets
+ *   ATTN_ERR_DEVICE_BOUNDS in the device error word (the output is then undefined).
+ *   Launches two kernels (split, combine). Returns ATTN_OK or a negative attn_status.
+ */
+int attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,
+                int num_seqs, int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
+                int num_blocks, float scale, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/*
+ * attn_decode_chunk_tokens -- keys per split-KV chunk attn_decode uses for these sizes
+ * (AK FlashDecoding: the chunk length of the split). Informational; 0 if invalid.
+ */
+int attn_decode_chunk_tokens(int num_seqs, int Hkv, int block_size, int max_blocks_per_seq);
+
+/*
+ * attn_get_device_error -- wait for `stream`, then read and clear the device error
+ * word of the current device. Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
+ * ATTN_ERR_DEVICE_BOUNDS, or ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+int attn_get_device_error(void* stream);
+
+/*
+ * attn_kv_layout_version -- identity of the paged-cache layout this build reads
+ * (MAK "Failure modes", page-table mismatch: encode layout identity).
+ * Version 1 = [num_blocks][Hkv][block_size][d], bf16, block_table int32 row-major.
+ */
+int attn_kv_layout_version(void);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char* attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

@@ -1,0 +1,124 @@
+"""CPU: the C-ABI library builds for sm_103a, loads without a GPU, exports every
+symbol include/attn.h declares, and rejects bad arguments before any launch."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_06_gb300 as eta
+from exact_tiled_attention_06_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    eta.build()
+    return eta.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_layout_version_and_status_strings(lib):
+    assert eta.attn_kv_layout_version() == 1
+    for code, name in binding.STATUS_NAMES.items():
+        assert eta.attn_status_string(code) == name
+
+
+FAKE = 0x7F0000000000  # never dereferenced: every call below fails validation first
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=64, scale=0.125,
+        causal=0, window=-1):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, window, None)
+
+
+def test_fwd_argument_validation(lib):
+    assert fwd(lib, q=None) == -1
+    assert fwd(lib, lse=None) == -1
+    assert fwd(lib, B=0) == -1
+    assert fwd(lib, Hq=3, Hkv=2) == -1       # Hq % Hkv != 0
+    assert fwd(lib, Nq=-1) == -1
+    assert fwd(lib, scale=0.0) == -1
+    assert fwd(lib, scale=float("nan")) == -1
+    assert fwd(lib, d=96) == -2
+    assert fwd(lib, d=256) == -2
+    assert fwd(lib, q=FAKE + 8) == -3        # not 16-byte aligned
+    assert fwd(lib, lse=FAKE + 2) == -3
+    assert fwd(lib, Nq=0) == 0               # nothing to do: no launch
+
+
+def dec(lib, ws_bytes=None, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, o=FAKE, lse=FAKE, S=4, Hq=8, Hkv=2, d=128,
+        bs=16, mb=64, nb=256, scale=0.1, ws=FAKE):
+    if ws_bytes is None:
+        ws_bytes = lib.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb)
+    return lib.attn_decode(q, kc, vc, bt, sl, o, lse, S, Hq, Hkv, d, bs, mb, nb, scale, ws, ws_bytes, None)
+
+
+def test_decode_argument_validation(lib):
+    assert dec(lib, q=None) == -1
+    assert dec(lib, bt=None) == -1
+    assert dec(lib, Hq=6, Hkv=4) == -1
+    assert dec(lib, nb=0) == -1
+    assert dec(lib, scale=-1.0) == -1
+    assert dec(lib, d=80) == -2
+    assert dec(lib, bs=8) == -2               # block size must be a multiple of 16
+    assert dec(lib, bs=24) == -2
+    assert dec(lib, bs=512) == -2
+    assert dec(lib, nb=1 << 26) == -2         # cache rows past 2^31
+    assert dec(lib, kc=FAKE + 4) == -3
+    assert dec(lib, ws_bytes=16) == -4        # workspace too small
+    assert dec(lib, ws=None) == -4
+    assert dec(lib, S=0) == 0                 # empty batch: no launch
+
+
+def test_workspace_size_matches_split_plan(lib):
+    S, Hq, Hkv, d, bs, mb = 64, 32, 8, 128, 16, 2048
+    chunk = eta.attn_decode_chunk_tokens(S, Hkv, bs, mb)
+    n_split = -(-mb * bs // chunk)
+    rows = n_split * S * Hq
+    want = -(-rows * 4 // 256) * 256 + rows * d * 4
+    assert eta.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb) == want
+    assert eta.attn_decode_workspace_size(S, Hq, Hkv, 96, bs, mb) == 0
+    assert chunk % bs == 0 and chunk % 16 == 0
+
+
+def test_split_plan_reproduces_flashdecoding_example(lib):
+    with open(os.path.join(GOLDEN, "flashdecoding_split_example.json")) as f:
+        g = json.load(f)
+    mb = g["kv_len"] // g["block_size"]
+    chunk = eta.attn_decode_chunk_tokens(g["batch"], g["heads"], g["block_size"], mb)
+    assert chunk == g["chunk"]
+    n_split = g["kv_len"] // chunk
+    assert n_split == g["chunks"]
+    assert g["batch"] * g["heads"] == g["units_without_split"]
+    assert (g["batch"] * g["heads"] * n_split) // g["units_without_split"] == g["parallelism_gain"]
+
+
+def test_product_path_has_no_oracle_import():
+    """The CUDA path never touches the CPU oracle (no fallback, no shared code)."""
+    pkg = os.path.dirname(eta.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), fn
+                assert "liboracle" not in text and "attn_oracle" not in text, fn

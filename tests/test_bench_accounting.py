@@ -1,0 +1,46 @@
+"""CPU: the benchmark's FLOP and byte accounting against the figures the pages print."""
+import json
+import os
+
+import bench
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "page_figures.json")
+
+
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def test_score_matrix_sizes_match_memory_table():
+    g = golden()["score_matrix_mib_bf16"]
+    for n, mib in g["values"].items():
+        assert round(bench.score_matrix_bytes(int(n)) / 2 ** 20, 1) == mib
+
+
+def test_score_matrix_mb_per_head():
+    g = golden()
+    assert bench.score_matrix_bytes(4096) / 2 ** 20 == g["score_matrix_mb_4096"]["value"]
+    assert round(bench.score_matrix_bytes(8192) / 1e6) == g["score_matrix_mb_8192"]["value"]
+
+
+def test_naive_traffic_and_time_estimate():
+    g = golden()["naive_prefill_traffic"]
+    b = bench.naive_score_traffic_bytes(g["N"], g["heads"], g["layers"])
+    assert int(b / 1e9) == g["gb"]
+    assert round(b / (g["hbm_tbs"] * 1e12) * 1e3) == g["ms"]
+
+
+def test_flops_per_head():
+    # 4 N^2 d per head without a mask; causal keeps N (N + 1) / 2 pairs
+    N, d = 8192, 128
+    assert bench.attention_flops(1, 1, N, N, d) == 4 * N * N * d
+    assert bench.attention_flops(1, 1, N, N, d, causal=True) == 4 * d * N * (N + 1) // 2
+    # window w (with causal): row i keeps min(i, w) + 1 keys
+    w = 1024
+    want = sum(min(i, w) + 1 for i in range(4096))
+    assert bench.allowed_pairs(4096, 4096, True, w) == want
+
+
+def test_decode_bytes():
+    assert bench.decode_kv_bytes([1024, 2048], 8, 128) == (1024 + 2048) * 8 * 128 * 2 * 2

@@ -1,0 +1,142 @@
+"""GPU parity: attn_decode (paged GQA split-KV decode) through the C ABI against the oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_06_gb300 as eta
+from exact_tiled_attention_06_gb300 import inputs
+from tests.gpu_util import check_attention, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    eta.build()
+    eta.load_library()
+
+
+def run_decode(x: inputs.PagedDecodeInputs, scale, workspace=None):
+    o, lse = eta.attn_decode(x.q.cuda(), x.k_cache.cuda(), x.v_cache.cuda(), x.block_table.cuda(),
+                             x.seq_lens.cuda(), scale=scale, workspace=workspace)
+    torch.cuda.synchronize()
+    assert eta.attn_get_device_error() == 0
+    return o, lse
+
+
+def oracle_decode(oracle, x: inputs.PagedDecodeInputs, scale, seqs=None):
+    """Oracle on the given sequences, with a compact copy of just their blocks
+    (the oracle then walks its own block table)."""
+    S = x.q.shape[0]
+    seqs = list(range(S)) if seqs is None else list(seqs)
+    bs = x.block_size
+    table = x.block_table.numpy()
+    lens = x.seq_lens.numpy()
+    used = []
+    for s in seqs:
+        n = (int(lens[s]) + bs - 1) // bs
+        used.extend(int(b) for b in table[s, :n])
+    used = sorted(set(used)) or [0]
+    remap = {b: i for i, b in enumerate(used)}
+    kc = f64(x.k_cache[used])
+    vc = f64(x.v_cache[used])
+    t2 = np.full((len(seqs), table.shape[1]), -1, dtype=np.int32)
+    for r, s in enumerate(seqs):
+        n = (int(lens[s]) + bs - 1) // bs
+        t2[r, :n] = [remap[int(b)] for b in table[s, :n]]
+    return oracle.attn_decode(f64(x.q[seqs]), kc, vc, t2, lens[seqs].astype(np.int32), scale)
+
+
+def case(oracle, S, Hq, Hkv, d, bs, lens=None, lo=1, hi=1, seed=0, poison=True, what=""):
+    x = inputs.decode_inputs(S, Hq, Hkv, d, bs, seq_lens=lens, len_lo=lo, len_hi=hi, seed=seed,
+                             extra_blocks=3, poison=poison)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_decode(x, scale)
+    o_ref, lse_ref = oracle_decode(oracle, x, scale)
+    check_attention(o, lse, o_ref, lse_ref, what)
+    return x, o, lse
+
+
+def test_c5_shape_reduced(oracle):
+    c = inputs.C5
+    case(oracle, 8, c.Hq, c.Hkv, c.d, c.block_size, lo=1, hi=3000, seed=1, what="C5-like")
+
+
+LENS = [0, 1, 15, 16, 17, 511, 512, 513, 1023, 1024, 1025, 2049]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_length_boundaries(oracle, d):
+    case(oracle, len(LENS), 8, 2, d, 16, lens=LENS, seed=2, what=f"lengths d={d}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (32, 8), (16, 2), (16, 1), (32, 1), (12, 4)])
+def test_group_sizes(oracle, Hq, Hkv):
+    case(oracle, 5, Hq, Hkv, 128, 16, lo=1, hi=1500, seed=Hq + Hkv, what=f"G={Hq // Hkv}")
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 256])
+def test_block_sizes(oracle, bs):
+    case(oracle, 6, 8, 2, 128, bs, lo=1, hi=1800, seed=bs, what=f"block_size={bs}")
+
+
+def test_nan_in_unowned_slots_is_never_used(oracle):
+    x, o, lse = case(oracle, 6, 8, 2, 128, 16, lens=[3, 17, 40, 100, 515, 1001], seed=3, poison=True,
+                     what="poisoned")
+    assert torch.isnan(x.k_cache.float()).any()  # the poison is really there
+    assert torch.all(torch.isfinite(o))
+
+
+def test_identity_table_matches_prefill_last_row():
+    """With an identity block table the cache is contiguous per sequence: decode of
+    one sequence equals the last row of causal prefill over the same keys."""
+    L, Hq, Hkv, d, bs = 777, 8, 2, 128, 16
+    x = inputs.decode_inputs(1, Hq, Hkv, d, bs, seq_lens=[L], seed=4, identity_table=True)
+    o_dec, lse_dec = run_decode(x, 1 / math.sqrt(d))
+    nblk = (L + bs - 1) // bs
+    k = x.k_cache[:nblk].permute(1, 0, 2, 3).reshape(Hkv, nblk * bs, d)[:, :L][None]
+    v = x.v_cache[:nblk].permute(1, 0, 2, 3).reshape(Hkv, nblk * bs, d)[:, :L][None]
+    q = torch.zeros(1, Hq, L, d, dtype=torch.bfloat16)
+    q[0, :, L - 1] = x.q[0]
+    o_pre, lse_pre = eta.attn_fwd(q.cuda(), k.contiguous().cuda(), v.contiguous().cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert (o_dec[0].float() - o_pre[0, :, L - 1].float()).abs().max().item() <= 2e-2
+    assert (lse_dec[0] - lse_pre[0, :, L - 1]).abs().max().item() <= 1e-3 * max(1.0, lse_pre.abs().max().item())
+
+
+def test_workspace_reuse_is_deterministic():
+    x = inputs.decode_inputs(4, 8, 2, 128, 16, len_lo=100, len_hi=3000, seed=5)
+    ws = torch.empty(eta.attn_decode_workspace_size(4, 8, 2, 128, 16, x.block_table.shape[1]), dtype=torch.uint8,
+                     device="cuda")
+    o1, l1 = run_decode(x, 0.1, workspace=ws)
+    o2, l2 = run_decode(x, 0.1, workspace=ws)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_out_of_range_block_id_sets_device_error():
+    x = inputs.decode_inputs(2, 8, 2, 128, 16, seq_lens=[100, 50], seed=6)
+    bt = x.block_table.clone()
+    nb = x.k_cache.shape[0]
+    bt[0, 2] = nb + 5  # inside sequence 0's length
+    eta.attn_decode(x.q.cuda(), x.k_cache.cuda(), x.v_cache.cuda(), bt.cuda(), x.seq_lens.cuda())
+    assert eta.attn_get_device_error() == -7
+    assert eta.attn_get_device_error() == 0  # read clears it
+    bt = x.block_table.clone()
+    bt[1, 0] = -1
+    eta.attn_decode(x.q.cuda(), x.k_cache.cuda(), x.v_cache.cuda(), bt.cuda(), x.seq_lens.cuda())
+    assert eta.attn_get_device_error() == -7
+
+
+def test_full_c5_sampled_sequences(oracle):
+    """The full decode workload as the bench runs it; sampled sequences against the oracle."""
+    c = inputs.C5
+    x = inputs.decode_config_inputs(c)
+    o, lse = run_decode(x, c.scale)
+    lens = x.seq_lens.numpy()
+    rng = np.random.default_rng(7)
+    seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens))} | set(int(s) for s in rng.integers(0, c.num_seqs, 3)))
+    o_ref, lse_ref = oracle_decode(oracle, x, c.scale, seqs)
+    check_attention(o.cpu()[seqs], lse.cpu()[seqs], o_ref, lse_ref, "C5 sampled")
+    assert torch.all(torch.isfinite(o))
