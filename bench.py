@@ -88,24 +88,31 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    "attn_fwd_sm103": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_decode_split_sm103": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is built from (so stale counters can be detected)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_06_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def load_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the kernel
-    sources changed after the counters were taken."""
+    """DRAM bytes per launch (read + write) from the committed ncu summary, or None when
+    the kernel's sources changed after the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         e = t.get(kernel)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(kernel):
             return float(e["bytes_per_launch"])
     except Exception:
         pass
@@ -113,16 +120,19 @@ def load_traffic(kernel: str):
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi; ``mark()`` brackets the
+    timed region so that only samples taken inside it are summarised."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.gpu = gpu_index
+        self.interval = interval_ms
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -130,16 +140,22 @@ class ClockSampler:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out,
-                                         stderr=subprocess.DEVNULL)
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
 
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.2)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -148,6 +164,7 @@ class ClockSampler:
             self.out.close()
 
     def summary(self):
+        import datetime
         if self.proc is None or not self.path:
             return None
         try:
@@ -155,26 +172,40 @@ class ClockSampler:
             os.unlink(self.path)
         except Exception:
             return None
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        inside, everything = [], []
         for r in rows:
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rec = (float(r[2]), float(r[3]), [n for n, v in zip(names, r[6:10]) if v.strip().lower() == "active"],
+                       float(r[4]) if r[4].strip() not in ("", "[N/A]") else None)
             except ValueError:
                 continue
-            for name, val in zip(names, r[5:9]):
-                if val.strip().lower() == "active":
-                    reasons.add(name)
-        if not sm:
+            everything.append(rec)
+            if self.t0 is not None and self.t1 is not None and self.t0 <= ts <= self.t1:
+                inside.append(rec)
+        use = inside or everything
+        if not use:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        reasons = sorted({n for rec in use for n in rec[2]})
+        power = [rec[3] for rec in use if rec[3] is not None]
+        return {"sm_mhz": float(np.median([rec[0] for rec in use])), "sm_max_mhz": float(max(rec[1] for rec in use)),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max(power) if power else None}
 
 
 # ----------------------------------------------------------------------------- our arm
+class Part:
+    """One half of the step: its inputs (pinned host + device), outputs and work units."""
+
+    def __init__(self, name, host, outputs, run, units, unit_scale, unit, launches):
+        self.name, self.host, self.outputs, self.run = name, host, outputs, run
+        self.units, self.unit_scale, self.unit, self.launches = units, unit_scale, unit, launches
+        self.dev = None
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -187,186 +218,187 @@ def run_ours(args, rank, world, local_rank):
     eta.build()
     eta.load_library()
     pc, dc = inputs.C3, inputs.C5
+    parts = []
 
-    # ---- synthetic inputs: pinned host copies (for the end-to-end leg) and HBM-resident copies
-    q_h, k_h, v_h = inputs.prefill_config_inputs(pc, seed=pc.seed + rank)
-    dx = inputs.decode_config_inputs(dc, seed=dc.seed + rank)
-    host = {"q": q_h, "k": k_h, "v": v_h, "dq": dx.q, "kc": dx.k_cache, "vc": dx.v_cache, "bt": dx.block_table,
-            "sl": dx.seq_lens}
-    host = {n: t.pin_memory() for n, t in host.items()}
-    d_in = {n: t.to(dev) for n, t in host.items()}
-    o = torch.empty_like(d_in["q"])
-    lse = torch.empty((pc.B, pc.Hq, pc.Nq), dtype=torch.float32, device=dev)
-    do = torch.empty_like(d_in["dq"])
-    dlse = torch.empty((dc.num_seqs, dc.Hq), dtype=torch.float32, device=dev)
-    mb = dx.block_table.shape[1]
-    ws = torch.empty(eta.attn_decode_workspace_size(dc.num_seqs, dc.Hq, dc.Hkv, dc.d, dc.block_size, mb),
-                     dtype=torch.uint8, device=dev)
+    if args.workload in ("both", "prefill"):
+        q_h, k_h, v_h = inputs.prefill_config_inputs(pc, seed=pc.seed + rank)
+        host = {n: t.pin_memory() for n, t in (("q", q_h), ("k", k_h), ("v", v_h))}
+        o = torch.empty(q_h.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((pc.B, pc.Hq, pc.Nq), dtype=torch.float32, device=dev)
+
+        def run_prefill(ins):
+            eta.attn_fwd(ins["q"], ins["k"], ins["v"], causal=pc.causal, window=pc.window, scale=pc.scale, out=o,
+                         lse=lse)
+
+        flops = attention_flops(pc.B, pc.Hq, pc.Nq, pc.Nk, pc.d, pc.causal, pc.window)
+        parts.append(Part("prefill", host, (o, lse), run_prefill, flops, 1e12, "TFLOP/s", 1))
+
+    if args.workload in ("both", "decode"):
+        if args.decode_seqs:
+            dx = inputs.decode_inputs(args.decode_seqs, dc.Hq, dc.Hkv, dc.d, dc.block_size, len_lo=dc.len_lo,
+                                      len_hi=dc.len_hi, seed=dc.seed + rank)
+        else:
+            dx = inputs.decode_config_inputs(dc, seed=dc.seed + rank)
+        S = dx.q.shape[0]
+        host = {n: t.pin_memory() for n, t in (("q", dx.q), ("kc", dx.k_cache), ("vc", dx.v_cache),
+                                                ("bt", dx.block_table), ("sl", dx.seq_lens))}
+        do = torch.empty(dx.q.shape, dtype=torch.bfloat16, device=dev)
+        dlse = torch.empty((S, dc.Hq), dtype=torch.float32, device=dev)
+        mb = dx.block_table.shape[1]
+        ws = torch.empty(eta.attn_decode_workspace_size(S, dc.Hq, dc.Hkv, dc.d, dc.block_size, mb),
+                         dtype=torch.uint8, device=dev)
+
+        def run_decode(ins):
+            eta.attn_decode(ins["q"], ins["kc"], ins["vc"], ins["bt"], ins["sl"], scale=dc.scale, workspace=ws,
+                            out=do, lse=dlse)
+
+        kv_bytes = decode_kv_bytes(dx.seq_lens.numpy(), dc.Hkv, dc.d)
+        part = Part("decode", host, (do, dlse), run_decode, kv_bytes, 1e9, "GB/s", 2)
+        part.extra = {"num_seqs": S, "sum_seq_len": int(dx.seq_lens.sum()), "workspace_bytes": int(ws.numel())}
+        parts.append(part)
+
+    for p in parts:
+        p.dev = {n: t.to(dev) for n, t in p.host.items()}
     stream = torch.cuda.current_stream()
-
-    def prefill(ins, out, out_lse):
-        eta.attn_fwd(ins["q"], ins["k"], ins["v"], causal=pc.causal, window=pc.window, scale=pc.scale, out=out,
-                     lse=out_lse)
-
-    def decode(ins, out, out_lse):
-        eta.attn_decode(ins["dq"], ins["kc"], ins["vc"], ins["bt"], ins["sl"], scale=dc.scale, workspace=ws,
-                        out=out, lse=out_lse)
-
-    flops = attention_flops(pc.B, pc.Hq, pc.Nq, pc.Nk, pc.d, pc.causal, pc.window)
-    kv_bytes = decode_kv_bytes(dx.seq_lens.numpy(), dc.Hkv, dc.d)
-    launches_per_step = 1 + 2  # prefill kernel; decode split + combine
 
     # ---- warm-up
     for _ in range(args.warmup):
-        prefill(d_in, o, lse)
-        decode(d_in, do, dlse)
+        for p in parts:
+            p.run(p.dev)
     torch.cuda.synchronize()
     err = eta.attn_get_device_error()
     if err != 0:
         raise RuntimeError(f"device error during warm-up: {eta.attn_status_string(err)}")
 
-    # ---- timed region: K steps, events around each kernel on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # ---- timed region: K steps; CUDA events around each part on the launching stream
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
+          for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
+        clocks.mark(True)
         t_start.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
-            prefill(d_in, o, lse)
-            ev[i][1].record(stream)
-            decode(d_in, do, dlse)
-            ev[i][2].record(stream)
+            for j, p in enumerate(parts):
+                ev[i][j][0].record(stream)
+                p.run(p.dev)
+                ev[i][j][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clocks.mark(False)
     if world > 1:
         dist.barrier()
     err = eta.attn_get_device_error()
     if err != 0:
         raise RuntimeError(f"device error in the timed region: {eta.attn_status_string(err)}")
     total_ms = t_start.elapsed_time(t_end)
-    pre_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
-    dec_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    part_ms = [np.array([ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)])
+               for j in range(len(parts))]
 
-    # ---- end to end through the public API with host buffers (copies inside the timed region)
-    h_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    h_do = torch.empty(do.shape, dtype=do.dtype, pin_memory=True)
-    h_dlse = torch.empty(dlse.shape, dtype=dlse.dtype, pin_memory=True)
-    pre_names, dec_names = ("q", "k", "v"), ("dq", "kc", "vc", "bt", "sl")
-    h2d_pre = sum(host[n].numel() * host[n].element_size() for n in pre_names)
-    h2d_dec = sum(host[n].numel() * host[n].element_size() for n in dec_names)
-    d2h_pre = o.numel() * 2 + lse.numel() * 4
-    d2h_dec = do.numel() * 2 + dlse.numel() * 4
-    e2e_steps = max(1, min(args.steps, 5))
-    e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for i in range(e2e_steps):
-        e_ev[i][0].record(stream)
-        for n in pre_names:
-            d_in[n].copy_(host[n], non_blocking=True)
-        prefill(d_in, o, lse)
-        h_o.copy_(o, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
-        e_ev[i][1].record(stream)
-        for n in dec_names:
-            d_in[n].copy_(host[n], non_blocking=True)
-        decode(d_in, do, dlse)
-        h_do.copy_(do, non_blocking=True)
-        h_dlse.copy_(dlse, non_blocking=True)
-        e_ev[i][2].record(stream)
-    torch.cuda.synchronize()
-    e2e_pre_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in e_ev]))
-    e2e_dec_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in e_ev]))
+    # ---- end to end through the public API with host buffers: every step copies its
+    #      inputs host->device, runs, and copies its outputs device->host (pinned memory)
+    e2e_ms = [0.0 for _ in parts]
+    e2e_steps = 0
+    h2d = d2h = 0
+    if not args.no_e2e:
+        outs_h = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in p.outputs] for p in parts]
+        h2d = sum(t.numel() * t.element_size() for p in parts for t in p.host.values())
+        d2h = sum(t.numel() * t.element_size() for p in parts for t in p.outputs)
+        e2e_steps = max(1, min(args.steps, 5))
+        e_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in parts]
+                for _ in range(e2e_steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(e2e_steps):
+            for j, p in enumerate(parts):
+                e_ev[i][j][0].record(stream)
+                for n, t in p.host.items():
+                    p.dev[n].copy_(t, non_blocking=True)
+                p.run(p.dev)
+                for t_h, t_d in zip(outs_h[j], p.outputs):
+                    t_h.copy_(t_d, non_blocking=True)
+                e_ev[i][j][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = [float(np.mean([e_ev[i][j][0].elapsed_time(e_ev[i][j][1]) for i in range(e2e_steps)]))
+                  for j in range(len(parts))]
 
     # ---- max over ranks
-    vals = torch.tensor([total_ms, pre_ms.mean(), dec_ms.mean(), e2e_pre_ms, e2e_dec_ms], dtype=torch.float64,
-                        device=dev)
+    vals = torch.tensor([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms, dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, pre_mean, dec_mean, e2e_pre_ms, e2e_dec_ms = (float(x) for x in vals.cpu())
+    vals = [float(x) for x in vals.cpu()]
+    total_ms, means, e2e_ms = vals[0], vals[1:1 + len(parts)], vals[1 + len(parts):]
     if rank != 0:
         return None
 
     peaks, peak_kind = load_peaks()
-    step_ms = total_ms / args.steps
-    # whole-job prefill throughput: all ranks' FLOPs over the max-over-ranks prefill time
-    pre_tflops = world * flops / (pre_mean * 1e-3) / 1e12
-    dec_gbs = world * kv_bytes / (dec_mean * 1e-3) / 1e9
-    achieved_pre = flops / (pre_mean * 1e-3) / 1e12  # one launch, one GPU
-    achieved_dec = kv_bytes / (dec_mean * 1e-3) / 1e9
+
+    def roofline(p, mean_ms, ms):
+        achieved = p.units / (mean_ms * 1e-3) / p.unit_scale  # one launch on one GPU
+        if p.name == "prefill":
+            rf = {"kernel": "attn_fwd_sm103<128>", "bound": "tensor", "achieved": round(achieved, 2),
+                  "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                  "frac": round(achieved / peaks["bf16_tflops"], 4),
+                  "peak_kind": f"{peak_kind} bf16 dense burst",
+                  "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                  "traffic": load_traffic("attn_fwd_sm103")}
+        else:
+            rf = {"kernel": "attn_decode_split_sm103<128> + attn_decode_combine_sm103<128>", "bound": "hbm",
+                  "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                  "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} HBM copy",
+                  "traffic": load_traffic("attn_decode_split_sm103")}
+        rf["ms_per_launch"] = round(mean_ms, 4)
+        rf["ms_p10_p50_p90"] = [round(float(np.percentile(ms, x)), 4) for x in (10, 50, 90)]
+        return rf
+
+    main_p, main_ms = parts[0], means[0]
+    value = world * main_p.units / (main_ms * 1e-3) / main_p.unit_scale
+    config = {"workload": " + ".join({"prefill": pc.name, "decode": dc.name}[p.name] for p in parts),
+              "l2": "inputs larger than L2 (prefill Q/K/V 192 MiB, decode KV ~4 GB); no flush",
+              "parallelism": f"replicas x{world}"}
+    for p in parts:
+        if p.name == "prefill":
+            config["prefill"] = {"B": pc.B, "Hq": pc.Hq, "Hkv": pc.Hkv, "Nq": pc.Nq, "Nk": pc.Nk, "d": pc.d,
+                                 "causal": pc.causal, "window": pc.window, "k_boost_frac": pc.k_boost_frac,
+                                 "flops_per_launch": p.units}
+        else:
+            config["decode"] = {"num_seqs": p.extra["num_seqs"], "Hq": dc.Hq, "Hkv": dc.Hkv, "d": dc.d,
+                                "block_size": dc.block_size, "len_range": [dc.len_lo, dc.len_hi],
+                                "sum_seq_len": p.extra["sum_seq_len"], "kv_bytes_per_launch": p.units}
     result = {
         "metric": METRIC,
-        "value": round(pre_tflops, 2),
-        "unit": "TFLOP/s",
+        "value": round(value, 2),
+        "unit": main_p.unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(step_ms, 4),
+        "ms_per_step": round(total_ms / args.steps, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": f"{pc.name} + {dc.name}",
-            "prefill": {"B": pc.B, "Hq": pc.Hq, "Hkv": pc.Hkv, "Nq": pc.Nq, "Nk": pc.Nk, "d": pc.d,
-                        "causal": pc.causal, "window": pc.window, "k_boost_frac": pc.k_boost_frac,
-                        "flops_per_launch": flops},
-            "decode": {"num_seqs": dc.num_seqs, "Hq": dc.Hq, "Hkv": dc.Hkv, "d": dc.d,
-                       "block_size": dc.block_size, "len_range": [dc.len_lo, dc.len_hi],
-                       "sum_seq_len": int(dx.seq_lens.sum()), "kv_bytes_per_launch": kv_bytes},
-            "l2": "inputs larger than L2 (prefill Q/K/V 192 MiB, decode KV ~4.4 GB); no flush",
-            "parallelism": f"replicas x{world}",
-        },
-        "roofline": {
-            "kernel": "attn_fwd_sm103<128>",
-            "bound": "tensor",
-            "achieved": round(achieved_pre, 2),
-            "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s",
-            "frac": round(achieved_pre / peaks["bf16_tflops"], 4),
-            "peak_kind": f"{peak_kind} bf16 dense burst",
-            "frac_of_sustained": round(achieved_pre / peaks["bf16_tflops_sustained"], 4),
-            "traffic": load_traffic("attn_fwd_sm103"),
-            "ms_per_launch": round(pre_mean, 4),
-            "ms_p10_p90": [round(float(np.percentile(pre_ms, 10)), 4), round(float(np.percentile(pre_ms, 90)), 4)],
-        },
-        "decode": {
-            "value": round(dec_gbs, 2),
-            "unit": "GB/s",
-            "roofline": {
-                "kernel": "attn_decode_split_sm103<128> + attn_decode_combine_sm103<128>",
-                "bound": "hbm",
-                "achieved": round(achieved_dec, 2),
-                "peak": peaks["hbm_gbs"],
-                "unit": "GB/s",
-                "frac": round(achieved_dec / peaks["hbm_gbs"], 4),
-                "peak_kind": f"{peak_kind} HBM copy",
-                "traffic": load_traffic("attn_decode_split_sm103"),
-                "ms_per_launch": round(dec_mean, 4),
-                "ms_p10_p90": [round(float(np.percentile(dec_ms, 10)), 4),
-                               round(float(np.percentile(dec_ms, 90)), 4)],
-            },
-            "workspace_bytes": int(ws.numel()),
-        },
-        "e2e": {
-            "value": round(world * flops / (e2e_pre_ms * 1e-3) / 1e12, 3),
-            "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d_pre + h2d_dec,
-            "d2h_bytes_per_step": d2h_pre + d2h_dec,
-            "decode_value": round(world * kv_bytes / (e2e_dec_ms * 1e-3) / 1e9, 2),
-            "decode_unit": "GB/s",
-            "ms_per_step": round(e2e_pre_ms + e2e_dec_ms, 3),
-            "steps": e2e_steps,
-        },
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks.summary(),
+        "config": config,
+        "roofline": roofline(main_p, main_ms, part_ms[0]),
     }
+    if len(parts) > 1:
+        p = parts[1]
+        result["decode"] = {"value": round(world * p.units / (means[1] * 1e-3) / p.unit_scale, 2), "unit": p.unit,
+                            "roofline": roofline(p, means[1], part_ms[1]),
+                            "workspace_bytes": p.extra["workspace_bytes"]}
+    if not args.no_e2e:
+        e2e = {"value": round(world * main_p.units / (e2e_ms[0] * 1e-3) / main_p.unit_scale, 3), "unit": main_p.unit,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(sum(e2e_ms), 3),
+               "steps": e2e_steps}
+        if len(parts) > 1:
+            e2e["decode_value"] = round(world * parts[1].units / (e2e_ms[1] * 1e-3) / parts[1].unit_scale, 2)
+            e2e["decode_unit"] = parts[1].unit
+        result["e2e"] = e2e
+    result["gpu_launches"] = sum(p.launches for p in parts) * args.steps
+    result["clocks"] = clocks.summary()
     return result
 
 
@@ -450,10 +482,15 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
+    ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
+                    help="profiling aid: run only one half of the step (the JSON line then omits the other)")
+    ap.add_argument("--decode-seqs", type=int, default=None,
+                    help="profiling aid: fewer decode sequences than the workload's 64")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
