@@ -25,7 +25,7 @@ STATUS_NAMES = {
 
 # Every symbol include/attn.h declares.
 EXPORTED = ("attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_decode_chunk_tokens",
-            "attn_get_device_error", "attn_kv_layout_version", "attn_status_string")
+            "attn_get_device_error", "attn_kv_layout_version", "attn_status_string", "attn_decode_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -65,6 +65,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_get_device_error.restype = i
         lib.attn_kv_layout_version.argtypes = []
         lib.attn_kv_layout_version.restype = i
+        lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        lib.attn_decode_noalloc.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -168,4 +170,32 @@ def attn_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, workspac
                                     _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode")
+    return out, lse
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=None, out=None, lse=None, stream=None):
+    """attn_decode for callers that cannot allocate device scratch: the split partials
+    live in a 64 MiB static array inside the library (calls must not overlap on the
+    GPU). Inputs and outputs as for attn_decode; ``out``/``lse`` are allocated here
+    only when not given."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    S, Hq, d = q.shape
+    nb, Hkv, bs, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape or block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("decode shapes disagree")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                            _ptr(seq_lens), _ptr(out), _ptr(lse), S, Hq, Hkv, d, bs,
+                                            block_table.shape[1], nb, float(scale), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_noalloc")
     return out, lse

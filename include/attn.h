@@ -121,6 +121,31 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache,
                 void* stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode without a caller-supplied workspace.
+ *
+ *   No counterpart in the pages: this is a deployment convenience. Some callers cannot
+ *   allocate device memory where they run decode (a serving runtime that reserved
+ *   nearly all of HBM for its KV-cache pool and forbids further cudaMalloc, or a
+ *   plugin running inside another framework's execution plan, where allocation calls
+ *   are not allowed). This variant keeps the split-KV partials in a static device
+ *   array inside libattn.so instead: 64 MiB, held on every GPU that loads the library
+ *   until the process exits. It allocates nothing; the caller still passes every input
+ *   and output, with the same meaning, layout and alignment as attn_decode.
+ *
+ *   Returns ATTN_ERR_WORKSPACE when attn_decode_workspace_size(...) for these sizes
+ *   exceeds 64 MiB. The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ *   capture. Every call shares the one array, so calls that overlap on the GPU (on
+ *   different streams, or from different threads) race and corrupt each other's
+ *   results; serialise them. The array keeps the last call's contents, and nothing in
+ *   it needs to start at zero: each call reads only partials it has written itself.
+ */
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,
+                        int num_seqs, int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
+                        int num_blocks, float scale, void* stream);
+
+/*
  * attn_decode_chunk_tokens -- keys per split-KV chunk attn_decode uses for these sizes
  * (AK FlashDecoding: the chunk length of the split). Informational; 0 if invalid.
  */
