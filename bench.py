@@ -90,7 +90,7 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "attn_fwd_sm103": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
-    "attn_decode_split_sm103": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_decode_sm103": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
 }
 
 
@@ -253,7 +253,7 @@ def run_ours(args, rank, world, local_rank):
                             out=do, lse=dlse)
 
         kv_bytes = decode_kv_bytes(dx.seq_lens.numpy(), dc.Hkv, dc.d)
-        part = Part("decode", host, (do, dlse), run_decode, kv_bytes, 1e9, "GB/s", 2)
+        part = Part("decode", host, (do, dlse), run_decode, kv_bytes, 1e9, "GB/s", 1)
         part.extra = {"num_seqs": S, "sum_seq_len": int(dx.seq_lens.sum()), "workspace_bytes": int(ws.numel())}
         parts.append(part)
 
@@ -346,10 +346,10 @@ def run_ours(args, rank, world, local_rank):
                   "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
                   "traffic": load_traffic("attn_fwd_sm103")}
         else:
-            rf = {"kernel": "attn_decode_split_sm103<128> + attn_decode_combine_sm103<128>", "bound": "hbm",
+            rf = {"kernel": "attn_decode_sm103<128>", "bound": "hbm",
                   "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                   "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} HBM copy",
-                  "traffic": load_traffic("attn_decode_split_sm103")}
+                  "traffic": load_traffic("attn_decode_sm103")}
         rf["ms_per_launch"] = round(mean_ms, 4)
         rf["ms_p10_p50_p90"] = [round(float(np.percentile(ms, x)), 4) for x in (10, 50, 90)]
         return rf
@@ -403,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_sample(heads=4, rows=None, seqs=2):
+def oracle_sample(heads=32, rows=None, seqs=4):
     """Time the fp64 oracle on a bounded sample of the same workload.
 
     Prefill: ``heads`` heads of the long causal workload, all rows (or only the last

@@ -38,12 +38,13 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 
 // Split-KV decode plan: the chunk length and the workspace carve-up.
 struct DecodePlan {
-    int chunk;          // keys per split (multiple of 16 and of block_size)
-    int n_split_max;    // splits of the longest possible sequence
-    int n_hgroups;      // groups of at most 16 query heads per kv head
-    size_t lse_offset;  // byte offset of the partial log-sums  [n_split_max][num_seqs][Hq] fp32
-    size_t o_offset;    // byte offset of the partial outputs   [n_split_max][num_seqs][Hq][d] fp32
-    size_t bytes;       // total workspace bytes
+    int chunk;              // keys per split (multiple of 16 and of block_size)
+    int n_split_max;        // splits of the longest possible sequence
+    int n_hgroups;          // groups of at most 16 query heads per kv head
+    size_t counters_bytes;  // work counter (8 bytes) + one completion counter per (sequence, head group)
+    size_t lse_offset;      // byte offset of the partial log-sums  [n_split_max][num_seqs][Hq] fp32
+    size_t o_offset;        // byte offset of the partial outputs   [n_split_max][num_seqs][Hq][d] fp32
+    size_t bytes;           // total workspace bytes
 };
 bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
                  DecodePlan* plan);

@@ -112,7 +112,8 @@ size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int bloc
  *   Cache slots past a sequence's length (the tail of its last block) are never used,
  *   whatever they hold. A block-table entry outside [0, num_blocks) sets
  *   ATTN_ERR_DEVICE_BOUNDS in the device error word (the output is then undefined).
- *   Launches two kernels (split, combine). Returns ATTN_OK or a negative attn_status.
+ *   Enqueues a 4-byte-granular memset of the workspace's counters and one kernel on
+ *   `stream`. Returns ATTN_OK or a negative attn_status.
  */
 int attn_decode(const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,
