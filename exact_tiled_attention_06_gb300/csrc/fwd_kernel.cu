@@ -258,15 +258,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
             // S_t = Q_t K^T: both operands K-major; a 16-wide k step is 32 bytes inside a
             // 128-byte swizzle row, and every 64 columns start a new box.
+            // Descriptors are built once; another k step, slot or tile only adds its byte
+            // offset / 16 to the start-address field (every address stays below 256 KB).
+            const uint64_t qdesc0 = smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t kdesc0 = smem_desc_sw128(sRing, 16, 1024);
+            const uint64_t vdesc0 = smem_desc_sw128(sRing, C::kBoxBytes, 1024);
             auto issue_qk = [&](int t, int slot) {
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * BN);
-                const uint32_t a0 = sQ + t * C::kTileBytes;
-                const uint32_t b0 = sRing + slot * C::kTileBytes;
+                const uint64_t qd = qdesc0 + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
+                const uint64_t kd = kdesc0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(d_tmem, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024),
-                           idesc_qk, kk > 0 ? 1u : 0u);
+                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
+                    mma_ss(d_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t (+)= P_t V: P from TMEM (8 columns = 16 bf16 keys per step); V is
@@ -275,10 +279,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             auto issue_pv = [&](int t, int slot, bool accumulate) {
                 const uint32_t d_tmem = tmem + C::kOCol + static_cast<uint32_t>(t * D);
                 const uint32_t a_tmem = tmem + static_cast<uint32_t>(t * BN);
-                const uint32_t v0 = sRing + slot * C::kTileBytes;
+                const uint64_t vd = vdesc0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(v0 + kk * 2048, C::kBoxBytes, 1024), idesc_pv,
+                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), idesc_pv,
                            (accumulate || kk > 0) ? 1u : 0u);
             };
 
@@ -394,13 +398,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int c = 0; c < BN; ++c)
                         if (c > hi_c || c < lo_c) s[c] = -INFINITY;
                 }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                for (int c = 4; c < BN; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                for (int c = 0; c < BN; c += 8) {
+                    mx0 = fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
                 }
                 const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
                 const bool need = m_cand > m + kRescaleThreshold || (m == -INFINITY && m_cand > -INFINITY);
@@ -413,18 +417,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 const float base = (m == -INFINITY) ? 0.0f : m;
                 float sum0 = 0.0f, sum1 = 0.0f;
-                uint32_t pk[BN / 2];
+                // p = 2^(s * scale * log2e - m) with paired fp32 FMAs; P as bf16 pairs over
+                // the first 64 columns of S_t
+                const uint64_t scale2 = f2pack(sl2, sl2);
+                const uint64_t nbase2 = f2pack(-base, -base);
+                uint64_t sum2 = f2pack(0.0f, 0.0f);
 #pragma unroll
-                for (int c = 0; c < BN; c += 2) {
-                    const float p0 = ex2_approx(fmaf(s[c], sl2, -base));
-                    const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -base));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[c / 2] = pack_bf16x2(p0, p1);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[BN / 4];
+#pragma unroll
+                    for (int c = h * BN / 2; c < (h + 1) * BN / 2; c += 2) {
+                        float t0, t1;
+                        f2unpack(f2fma(f2pack(s[c], s[c + 1]), scale2, nbase2), t0, t1);
+                        const float p0 = ex2_approx(t0);
+                        const float p1 = ex2_approx(t1);
+                        sum2 = f2add(sum2, f2pack(p0, p1));
+                        pk[(c - h * BN / 2) / 2] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(s_tmem + 32 * h, pk);
                 }
-                // P (bf16 pairs) over the first 64 columns of S_t
-                tmem_st32(s_tmem, pk);
-                tmem_st32(s_tmem + 32, pk + 32);
+                f2unpack(sum2, sum0, sum1);
                 l = l * alpha + (sum0 + sum1);
                 if (rescale && n_act > 0) {
                     // O <- alpha * O. The previous P V has finished: it was issued before

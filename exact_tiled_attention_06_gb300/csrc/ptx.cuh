@@ -13,20 +13,14 @@ namespace attn {
 constexpr unsigned kDevErrTimeout = 6u;
 constexpr unsigned kDevErrBounds = 7u;
 
-// Every mbarrier wait gives up after this long (wall clock, %globaltimer in ns)
-// and reports a timeout instead of spinning forever.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Every mbarrier wait gives up after this many SM clock cycles (about 2 s at 2 GHz) and
+// reports a timeout instead of spinning forever. The SM-local cycle counter is used
+// because reading it costs a few cycles, unlike the global nanosecond timer.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 // Record a device-detected problem in the library's error word (first one wins).
@@ -74,24 +68,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0u;
 }
 
-// Wait for the phase of `bar` with the given parity to complete. Gives up (returns
-// false) when *abort is set by another thread of the block, or after kWaitLimitNs,
-// in which case it sets *abort and reports a timeout. `abort` may be null.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* err)
+// Slow path of mbar_wait: spin with a time limit.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                   unsigned* err)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (clock64() - t0 > kWaitLimitCycles) {
             if (abort) *abort = 1;
             report_error(err, kDevErrTimeout);
             return false;
         }
     }
+}
+
+// Wait for the phase of `bar` with the given parity to complete. Gives up (returns
+// false) when *abort is set by another thread of the block, or after kWaitLimitCycles,
+// in which case it sets *abort and reports a timeout. `abort` may be null. The first
+// test is inline: a wait on a phase that has already completed costs a few cycles.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, err);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -233,6 +235,41 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r)
 __device__ __forceinline__ void tmem_st_wait()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- packed fp32 pairs
+// Two fp32 lanes in one 64-bit register (low = first), for the paired FMA/ADD units.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // ---------------------------------------------------------------- misc math
