@@ -77,6 +77,23 @@ def prefill_io_bytes(B, Hq, Hkv, Nq, Nk, d) -> int:
     return 2 * d * (B * Hq * Nq * 2 + B * Hkv * Nk * 2) + 4 * B * Hq * Nq
 
 
+# ----------------------------------------------------------------------------- multi-rank
+def reduce_max(vals, world: int, device):
+    """Element-wise maximum of per-rank timings across all ranks (identity for one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_ms: float, unit_scale: float) -> float:
+    """Replicas: every rank does the same work; the job's rate is all ranks' units over the
+    slowest rank's time."""
+    return world * units_per_rank / (max_ms * 1e-3) / unit_scale
+
+
 # ----------------------------------------------------------------------------- environment
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -326,10 +343,7 @@ def run_ours(args, rank, world, local_rank):
                   for j in range(len(parts))]
 
     # ---- max over ranks
-    vals = torch.tensor([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms, dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    vals = [float(x) for x in vals.cpu()]
+    vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms, world, dev)
     total_ms, means, e2e_ms = vals[0], vals[1:1 + len(parts)], vals[1 + len(parts):]
     if rank != 0:
         return None
@@ -355,7 +369,7 @@ def run_ours(args, rank, world, local_rank):
         return rf
 
     main_p, main_ms = parts[0], means[0]
-    value = world * main_p.units / (main_ms * 1e-3) / main_p.unit_scale
+    value = whole_job_rate(main_p.units, world, main_ms, main_p.unit_scale)
     config = {"workload": " + ".join({"prefill": pc.name, "decode": dc.name}[p.name] for p in parts),
               "l2": "inputs larger than L2 (prefill Q/K/V 192 MiB, decode KV ~4 GB); no flush",
               "parallelism": f"replicas x{world}"}
@@ -386,15 +400,15 @@ def run_ours(args, rank, world, local_rank):
     }
     if len(parts) > 1:
         p = parts[1]
-        result["decode"] = {"value": round(world * p.units / (means[1] * 1e-3) / p.unit_scale, 2), "unit": p.unit,
+        result["decode"] = {"value": round(whole_job_rate(p.units, world, means[1], p.unit_scale), 2), "unit": p.unit,
                             "roofline": roofline(p, means[1], part_ms[1]),
                             "workspace_bytes": p.extra["workspace_bytes"]}
     if not args.no_e2e:
-        e2e = {"value": round(world * main_p.units / (e2e_ms[0] * 1e-3) / main_p.unit_scale, 3), "unit": main_p.unit,
+        e2e = {"value": round(whole_job_rate(main_p.units, world, e2e_ms[0], main_p.unit_scale), 3), "unit": main_p.unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(sum(e2e_ms), 3),
                "steps": e2e_steps}
         if len(parts) > 1:
-            e2e["decode_value"] = round(world * parts[1].units / (e2e_ms[1] * 1e-3) / parts[1].unit_scale, 2)
+            e2e["decode_value"] = round(whole_job_rate(parts[1].units, world, e2e_ms[1], parts[1].unit_scale), 2)
             e2e["decode_unit"] = parts[1].unit
         result["e2e"] = e2e
     result["gpu_launches"] = sum(p.launches for p in parts) * args.steps
