@@ -21,6 +21,8 @@ What each function follows (pages by title and section):
   "Online softmax makes tiling exact".
 * ``attn_fwd_split`` -- per-chunk partials merged with the two-partial
   rescaling of "Attention kernels" (FlashDecoding).
+* ``attn_bwd`` -- gradients of attention by the chain rule with the probability rows
+  recomputed ("Modern attention kernels", "Backward pass recomputes scores").
 * ``attn_decode`` -- one query per sequence over a paged cache, addressed with
   the block-table formula of "Modern attention kernels",
   "Paged attention changes addressing".
@@ -74,9 +76,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                                                                  c_int, c_int]
     lib.oracle_attn_fwd_split.argtypes = [_D, _D, _D, _D, _D] + [c_int] * 6 + [c_double, c_int, c_int, c_int]
     lib.oracle_attn_decode.argtypes = [_D, _D, _D, _I32, _I32, _D, _D] + [c_int] * 7 + [c_double]
+    lib.oracle_attn_bwd.argtypes = [_D] * 7 + [c_int] * 6 + [c_double, c_int, c_int]
     lib.oracle_num_threads.argtypes = []
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows, lib.oracle_attn_fwd_blocked,
-              lib.oracle_attn_fwd_split, lib.oracle_attn_decode, lib.oracle_num_threads):
+              lib.oracle_attn_fwd_split, lib.oracle_attn_decode, lib.oracle_attn_bwd, lib.oracle_num_threads):
         f.restype = c_int
     return lib
 
@@ -171,6 +174,17 @@ class Oracle:
                "oracle_attn_fwd_split")
         return o, lse
 
+    def attn_bwd(self, q, k, v, dout, scale, causal=False, window=-1):
+        """Gradients (dq, dk, dv) of sum(dout * O) for O = attention(q, k, v), materialised."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, Hq, Hkv, Nq, Nk, d = _shapes(q, k, v)
+        if dout.shape != q.shape:
+            raise ValueError("dout must have the shape of q")
+        dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+        _check(self.lib.oracle_attn_bwd(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), B, Hq, Hkv, Nq,
+                                        Nk, d, float(scale), int(bool(causal)), int(window)), "oracle_attn_bwd")
+        return dq, dk, dv
+
     def attn_decode(self, q, k_cache, v_cache, block_table, seq_lens, scale):
         """Paged one-query decode. q [S][Hq][d]; caches [num_blocks][Hkv][bs][d];
         block_table int32 [S][max_blocks]; seq_lens int32 [S]. Returns (o [S][Hq][d], lse [S][Hq])."""
@@ -218,6 +232,10 @@ def attn_fwd_split(*a, **kw):
 
 def attn_decode(*a, **kw):
     return default().attn_decode(*a, **kw)
+
+
+def attn_bwd(*a, **kw):
+    return default().attn_bwd(*a, **kw)
 
 
 def num_threads() -> int:

@@ -418,6 +418,96 @@ int oracle_attn_decode(const double* q, const double* k_cache, const double* v_c
     return err;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Backward pass, materialised.                                                */
+/* [MAK] "Backward pass recomputes scores" and [IOA] (backward paragraph): the  */
+/*   gradients are formed from the same scores; here every row's score and     */
+/*   probability rows are materialised again from Q, K, V (no saved P).        */
+/* Chain rule of O = softmax(S) V with S = scale * Q K^T, for an upstream dO:   */
+/*   dV_j  = sum_i P_ij dO_i                                                   */
+/*   dP_ij = dO_i . v_j                                                        */
+/*   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)      (softmax Jacobian)            */
+/*   dQ_i  = scale * sum_j dS_ij k_j,   dK_j = scale * sum_i dS_ij q_i          */
+/* Masked pairs have P_ij = 0 and contribute nothing. With GQA, a kv head's     */
+/* dK, dV sum over the query heads that read it.                               */
+/* dout, dq: [B][Hq][Nq][d]; dk, dv: [B][Hkv][Nk][d].                           */
+/* ------------------------------------------------------------------------- */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                    double scale, int causal, int window)
+{
+    if (check_dims(B, Hq, Hkv, Nq, Nk, d)) return ORACLE_EINVAL;
+    int G = Hq / Hkv;
+    memset(dq, 0, sizeof(double) * (size_t)B * Hq * Nq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* dp = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        if (!s || !p || !dp) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+            /* one (batch, kv head) per iteration: its dK, dV are written by one thread */
+#pragma omp for schedule(dynamic, 1)
+            for (long bk = 0; bk < (long)B * Hkv; ++bk) {
+                long b = bk / Hkv, hk = bk % Hkv;
+                const double* kh = k + (bk * (long)Nk * d);
+                const double* vh = v + (bk * (long)Nk * d);
+                double* dkh = dk + (bk * (long)Nk * d);
+                double* dvh = dv + (bk * (long)Nk * d);
+                for (long h = hk * G; h < (hk + 1) * G; ++h) {
+                    for (long i = 0; i < Nq; ++i) {
+                        const double* qi = q + (((b * Hq + h) * (long)Nq + i) * d);
+                        const double* doi = dout + (((b * Hq + h) * (long)Nq + i) * d);
+                        double* dqi = dq + (((b * Hq + h) * (long)Nq + i) * d);
+                        /* probability row, exactly as in the forward */
+                        double m = -INFINITY;
+                        for (long j = 0; j < Nk; ++j) {
+                            s[j] = key_allowed(i, j, Nq, Nk, causal, window) ? scale * dot(qi, kh + j * d, d)
+                                                                             : -INFINITY;
+                            if (s[j] > m) m = s[j];
+                        }
+                        if (m == -INFINITY) continue;  /* empty row: no gradient flows */
+                        double l = 0.0;
+                        for (long j = 0; j < Nk; ++j) {
+                            p[j] = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - m);
+                            l += p[j];
+                        }
+                        for (long j = 0; j < Nk; ++j) p[j] /= l;
+                        /* dP row and the row term sum_k P_ik dP_ik */
+                        double row = 0.0;
+                        for (long j = 0; j < Nk; ++j) {
+                            dp[j] = (p[j] == 0.0) ? 0.0 : dot(doi, vh + j * d, d);
+                            row += p[j] * dp[j];
+                        }
+                        for (long j = 0; j < Nk; ++j) {
+                            if (p[j] == 0.0) continue;
+                            double ds = p[j] * (dp[j] - row);
+                            const double* kj = kh + j * d;
+                            double* dkj = dkh + j * d;
+                            double* dvj = dvh + j * d;
+                            for (int t = 0; t < d; ++t) {
+                                dvj[t] += p[j] * doi[t];
+                                dqi[t] += scale * ds * kj[t];
+                                dkj[t] += scale * ds * qi[t];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        free(s);
+        free(p);
+        free(dp);
+    }
+    return err;
+}
+
 /* Number of OpenMP threads the oracle will use (reported beside CPU timings). */
 int oracle_num_threads(void)
 {

@@ -24,6 +24,11 @@ What each pin rests on (pages by title and section):
   attention kernels", "Paged attention changes addressing").
 * an independent numpy brute force on tiny inputs.
 * the hand-derived three-key example in ``tests/golden/three_keys.json``.
+* backward ("Modern attention kernels", "Backward pass recomputes scores"): central
+  finite differences of sum(dO * O) through the forward oracle; torch autograd of a
+  plain softmax attention on tiny inputs; the exact invariants sum_j dK_j = 0 (softmax
+  is shift invariant per row) and sum_j dV_j = sum over non-empty rows of dO_i; GQA
+  gradients equal the summed gradients of duplicated heads.
 """
 from __future__ import annotations
 
@@ -311,6 +316,85 @@ def pin_large_logits_and_late_maximum(orc):
         _close(lb, lse, 1e-12, f"late-max blocked lse bc={bc}")
 
 
+BWD_MASKS = [(6, 6, False, -1), (6, 6, True, -1), (4, 7, True, -1), (7, 4, True, -1), (6, 6, True, 2)]
+
+
+def pin_bwd_finite_differences(orc):
+    h = 1e-6
+    for mi, (Nq, Nk, causal, window) in enumerate(BWD_MASKS):
+        q, k, v = _qkv(1400 + mi, 1, 2, 1, Nq, Nk, 3)
+        do = _rng(1450 + mi).standard_normal(q.shape)
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, 0.7, causal, window)
+
+        def loss(q_, k_, v_):
+            o, _ = orc.attn_fwd(q_, k_, v_, 0.7, causal, window)
+            return float((o * do).sum())
+
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp = x.copy(); xp[idx] += h
+                xm = x.copy(); xm[idx] -= h
+                args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+                args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            err = np.max(np.abs(num - g))
+            assert err <= 1e-7 * max(1.0, np.max(np.abs(g))), f"d{name} finite differences mask{mi}: {err:.2e}"
+
+
+def pin_bwd_torch_autograd(orc):
+    import torch
+    for mi, (Nq, Nk, causal, window) in enumerate(BWD_MASKS):
+        q, k, v = _qkv(1500 + mi, 2, 4, 2, Nq, Nk, 5)
+        do = _rng(1550 + mi).standard_normal(q.shape)
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, 0.45, causal, window)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        kk = tk.repeat_interleave(2, dim=1)
+        vv = tv.repeat_interleave(2, dim=1)
+        sc = 0.45 * tq @ kk.transpose(-1, -2)
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        diag = i + (Nk - Nq)
+        keep = torch.ones(Nq, Nk, dtype=torch.bool)
+        if causal:
+            keep &= j <= diag
+        if window >= 0:
+            keep &= j >= diag - window
+        sc = sc.masked_fill(~keep, float("-inf"))
+        p = torch.softmax(sc, dim=-1)
+        p = torch.nan_to_num(p, nan=0.0)  # rows with no key
+        o = p @ vv
+        (o * torch.tensor(do)).sum().backward()
+        for name, mine, ref in (("q", dq, tq.grad), ("k", dk, tk.grad), ("v", dv, tv.grad)):
+            assert np.max(np.abs(mine - ref.numpy())) <= 1e-12 * max(1.0, float(ref.abs().max())), \
+                f"d{name} autograd mask{mi}"
+
+
+def pin_bwd_invariants(orc):
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        q, k, v = _qkv(1600 + mi, 1, 4, 2, Nq, Nk, 8)
+        do = _rng(1650 + mi).standard_normal(q.shape)
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, 0.3, causal, window)
+        assert np.max(np.abs(dk.sum(axis=2))) <= 1e-11 * max(1.0, np.max(np.abs(dk))), f"sum dK mask{mi}"
+        nonempty = np.array([_allowed_range(i, Nq, Nk, causal, window)[1] >
+                             _allowed_range(i, Nq, Nk, causal, window)[0] for i in range(Nq)])
+        for hk in range(2):
+            want = do[0, 2 * hk:2 * hk + 2][:, nonempty].sum(axis=(0, 1))
+            assert np.max(np.abs(dv[0, hk].sum(axis=0) - want)) <= 1e-11, f"sum dV mask{mi}"
+
+
+def pin_bwd_gqa_equals_duplicated_heads(orc):
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS[:5]):
+        q, k, v = _qkv(1700 + mi, 1, 6, 2, Nq, Nk, 4)
+        do = _rng(1750 + mi).standard_normal(q.shape)
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, 0.3, causal, window)
+        kd, vd = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+        dq2, dk2, dv2 = orc.attn_bwd(q, kd, vd, do, 0.3, causal, window)
+        _close(dq, dq2, 1e-12, f"GQA dq mask{mi}")
+        _close(dk, dk2.reshape(1, 2, 3, Nk, 4).sum(axis=2), 1e-12, f"GQA dk mask{mi}")
+        _close(dv, dv2.reshape(1, 2, 3, Nk, 4).sum(axis=2), 1e-12, f"GQA dv mask{mi}")
+
+
 ALL_PINS = [
     pin_blocked_equals_materialised,
     pin_split_equals_unsplit,
@@ -326,4 +410,8 @@ ALL_PINS = [
     pin_numpy_bruteforce,
     pin_golden_three_keys,
     pin_large_logits_and_late_maximum,
+    pin_bwd_finite_differences,
+    pin_bwd_torch_autograd,
+    pin_bwd_invariants,
+    pin_bwd_gqa_equals_duplicated_heads,
 ]

@@ -24,8 +24,14 @@ MUTANTS = [
     ("decode_no_head_offset", "physical * block_stride + hk * (long)block_size * d + offset * token_stride",
      "physical * block_stride + offset * token_stride"),
     ("decode_offset_by_block", "long offset = t % block_size;", "long offset = t / block_size;"),
-    ("no_final_divide", "for (long j = 0; j < Nk; ++j) p[j] /= l;", ""),
+    ("no_final_divide", "for (long j = 0; j < Nk; ++j) p[j] /= l;\n    /* O = P V */", "/* O = P V */"),
+    ("bwd_no_normalisation", "for (long j = 0; j < Nk; ++j) p[j] /= l;\n                        /* dP row",
+     "/* dP row"),
     ("blocked_sum_not_corrected", "l[i - i0] = corr * l[i - i0] + lsum;", "l[i - i0] = l[i - i0] + lsum;"),
+    ("bwd_dropped_row_term", "double ds = p[j] * (dp[j] - row);", "double ds = p[j] * dp[j];"),
+    ("bwd_dk_from_k", "dkj[t] += scale * ds * qi[t];", "dkj[t] += scale * ds * kj[t];"),
+    ("bwd_dq_missing_scale", "dqi[t] += scale * ds * kj[t];", "dqi[t] += ds * kj[t];"),
+    ("bwd_dv_from_dp", "dvj[t] += p[j] * doi[t];", "dvj[t] += dp[j] * doi[t];"),
 ]
 
 
