@@ -24,8 +24,9 @@ STATUS_NAMES = {
 }
 
 # Every symbol include/attn.h declares.
-EXPORTED = ("attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_decode_chunk_tokens",
-            "attn_get_device_error", "attn_kv_layout_version", "attn_status_string", "attn_decode_noalloc")
+EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
+            "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
+            "attn_decode_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -55,6 +56,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         lib.attn_fwd.restype = i
+        lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+        lib.attn_bwd_workspace_size.restype = sz
+        lib.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, i, vp, sz, vp]
+        lib.attn_bwd.restype = i
         lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
         lib.attn_decode_workspace_size.restype = sz
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, vp]
@@ -131,6 +136,43 @@ def attn_fwd(q, k, v, causal=False, window=-1, scale=None, out=None, lse=None, s
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse
+
+
+def attn_bwd_workspace_size(B, Hq, Nq, d) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, Hq, Nq, d))
+
+
+def attn_bwd(q, k, v, o, dout, lse, causal=False, window=-1, scale=None, workspace=None, dq=None, dk=None,
+             dv=None, stream=None):
+    """Attention backward. q, o, dout [B][Hq][Nq][d] bf16; k, v [B][Hkv][Nk][d] bf16;
+    lse fp32 [B][Hq][Nq] (o and lse from attn_fwd). Returns (dq, dk, dv) in bf16."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, name, torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk_ = k.shape
+    if Bk != B or dk_ != d or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("backward shapes disagree")
+    if lse.shape != (B, Hq, Nq):
+        raise ValueError("lse must be [B][Hq][Nq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_bwd_workspace_size(B, Hq, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need(dq, "dq", torch.bfloat16, 4)
+    _need(dk, "dk", torch.bfloat16, 4)
+    _need(dv, "dv", torch.bfloat16, 4)
+    rc = load_library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)), int(window),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_decode_workspace_size(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_seq) -> int:

@@ -128,6 +128,44 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       static_cast<cudaStream_t>(stream), err);
 }
 
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d)
+{
+    if (B <= 0 || Hq <= 0 || Nq < 0 || (d != 64 && d != 128)) return 0;
+    if (static_cast<long long>(B) * Hq > INT32_MAX / 2) return 0;
+    return bwd_layout(B, Hq, Nq, d).bytes;
+}
+
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                      int d, float scale, int causal, int window, void* workspace, size_t workspace_bytes,
+                      void* stream)
+{
+    // ---- arguments (no CUDA call before these checks)
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return kErrInvalidArg;
+    if (Nq > 0 && (!q || !o || !dout || !lse || !dq)) return kErrInvalidArg;
+    if (Nk > 0 && (!k || !v || !dk || !dv)) return kErrInvalidArg;
+    if (Hq % Hkv != 0) return kErrInvalidArg;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return kErrInvalidArg;
+    if (static_cast<long long>(B) * Hq > INT32_MAX / 2 || static_cast<long long>(B) * Hkv > INT32_MAX / 2)
+        return kErrInvalidArg;
+    if (d != 64 && d != 128) return kErrUnsupported;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned4(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return kErrMisaligned;  // null is aligned
+    if (Nq == 0 && Nk == 0) return kOk;
+    const BwdLayout lay = bwd_layout(B, Hq, Nq, d);
+    if (!workspace || workspace_bytes < lay.bytes) return kErrWorkspace;
+    if (!aligned16(workspace)) return kErrMisaligned;
+    // ---- device
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc != kOk) return rc;
+    unsigned* err = device_error_word();
+    if (!err) return kErrCuda;
+    return launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, window, workspace,
+                      static_cast<cudaStream_t>(stream), err);
+}
+
 ATTN_API size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int block_size,
                                            int max_blocks_per_seq)
 {

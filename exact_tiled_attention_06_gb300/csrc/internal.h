@@ -55,4 +55,18 @@ int launch_decode(const void* q, const void* k_cache, const void* v_cache, const
                   int block_size, int max_blocks_per_seq, int num_blocks, float scale, void* workspace,
                   const DecodePlan& plan, cudaStream_t stream, unsigned* err);
 
+// Backward workspace: D_i [B][Hq][Nq] fp32 at dvec_offset, then the fp32 dQ accumulator
+// [B][Hq][Nq][d] at dq_offset (256-byte aligned).
+struct BwdLayout {
+    size_t dvec_offset;
+    size_t dq_offset;
+    size_t bytes;
+};
+BwdLayout bwd_layout(int B, int Hq, int Nq, int d);
+
+// Backward (implemented in bwd_kernel.cu). Arguments are already validated.
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+               void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+               int window, void* workspace, cudaStream_t stream, unsigned* err);
+
 }  // namespace attn

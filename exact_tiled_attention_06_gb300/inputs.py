@@ -99,6 +99,13 @@ def prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=0, k_boost_frac=0.0, k_boost=2.0)
     return q, k, v
 
 
+def grad_output(B, Hq, Nq, d, seed=0):
+    """Return a host bf16 upstream gradient dO [B][Hq][Nq][d] (standard normal entries,
+    drawn from a generator seeded apart from q, k, v)."""
+    gen = torch.Generator().manual_seed(int(seed) * 7919 + 104729)
+    return _bf16_normal(gen, (B, Hq, Nq, d))
+
+
 def prefill_config_inputs(cfg: PrefillConfig, seed=None):
     return prefill_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.Nq, cfg.Nk, cfg.d,
                           seed=cfg.seed if seed is None else seed, k_boost_frac=cfg.k_boost_frac)

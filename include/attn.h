@@ -39,7 +39,7 @@ typedef enum attn_status {
     ATTN_ERR_INVALID_ARG = -1,     /* null pointer, bad size, Hq % Hkv != 0, scale <= 0 ... */
     ATTN_ERR_UNSUPPORTED = -2,     /* d not in {64,128}, block_size not a multiple of 16, non-sm_103 device */
     ATTN_ERR_MISALIGNED = -3,      /* a pointer is not 16-byte aligned */
-    ATTN_ERR_WORKSPACE = -4,       /* decode workspace missing or smaller than attn_decode_workspace_size() */
+    ATTN_ERR_WORKSPACE = -4,       /* workspace missing or smaller than the *_workspace_size() figure */
     ATTN_ERR_LAUNCH = -5,          /* a kernel launch failed */
     ATTN_ERR_DEVICE_TIMEOUT = -6,  /* a bounded pipeline wait inside a kernel ran out of time */
     ATTN_ERR_DEVICE_BOUNDS = -7,   /* a kernel met a block-table entry outside [0, num_blocks) */
@@ -71,6 +71,48 @@ typedef enum attn_status {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
              int causal, int window, void* stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: D_i = rowsum(dO o O) in
+ * fp32 [B][Hq][Nq] (256-byte aligned), then an fp32 dQ accumulator [B][Hq][Nq][d].
+ * Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d);
+
+/*
+ * attn_bwd -- gradients of attention: dQ, dK, dV of L = sum(dO o O) for the O that
+ *   attn_fwd computes from the same q, k, v, scale, causal and window.
+ *
+ *   MAK "Backward pass recomputes scores" (the forward keeps only the per-row
+ *   statistic; the backward recomputes score tiles from Q, K, V instead of reading a
+ *   stored P); IOA (only the softmax row statistics are saved, P is recomputed block
+ *   by block in the backward); AK (recomputation instead of materialising attention).
+ *   With P_ij = exp(scale q_i.k_j - lse_i) (0 where masked):
+ *     dV_j = sum_i P_ij dO_i,   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,
+ *     dS_ij = P_ij (dP_ij - D_i),   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i.
+ *
+ *   q, o, dout : bf16 [B][Hq][Nq][d]     (input) o and lse as written by attn_fwd
+ *   k, v       : bf16 [B][Hkv][Nk][d]    (input)
+ *   lse        : fp32 [B][Hq][Nq]        (input) from attn_fwd
+ *   dq         : bf16 [B][Hq][Nq][d]     (output)
+ *   dk, dv     : bf16 [B][Hkv][Nk][d]    (output) summed over the Hq/Hkv query heads
+ *                                         that share each kv head
+ *   scale, causal, window: as for attn_fwd.  A row with no allowed key (lse = -inf)
+ *   contributes nothing and gets dQ = 0.
+ *   P and dS are rounded to bf16 before they enter the tensor-core products, with fp32
+ *   accumulation (the same precision as the forward's P V product).
+ *   workspace : device scratch of at least attn_bwd_workspace_size(B, Hq, Nq, d) bytes,
+ *               16-byte aligned; no initialisation needed; clobbered. Two calls that
+ *               share a workspace must not overlap on the device. No output may alias
+ *               an input or the workspace.
+ *   Sizes: as for attn_fwd; Nq = 0 gives dK = dV = 0, Nk = 0 gives dQ = 0.
+ *   Enqueues three kernels on `stream` (statistics, main, dQ conversion).
+ *   Returns ATTN_OK or a negative attn_status.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv,
+             int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+             int causal, int window, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_decode_workspace_size -- bytes of scratch attn_decode needs for these sizes.

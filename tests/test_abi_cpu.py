@@ -66,6 +66,44 @@ def test_fwd_argument_validation(lib):
     assert fwd(lib, Nq=0) == 0               # nothing to do: no launch
 
 
+def bwd(lib, ws_bytes=None, q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, Hq=4,
+        Hkv=2, Nq=200, Nk=300, d=128, scale=0.1, causal=1, window=-1, ws=FAKE):
+    if ws_bytes is None:
+        ws_bytes = lib.attn_bwd_workspace_size(B, Hq, Nq, d)
+    return lib.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, window, ws, ws_bytes,
+                        None)
+
+
+def test_bwd_argument_validation(lib):
+    assert bwd(lib, q=None) == -1
+    assert bwd(lib, do=None) == -1
+    assert bwd(lib, dk=None) == -1
+    assert bwd(lib, Hq=3, Hkv=2) == -1
+    assert bwd(lib, Nk=-1) == -1
+    assert bwd(lib, scale=float("inf")) == -1
+    assert bwd(lib, d=96) == -2
+    assert bwd(lib, dq=FAKE + 2) == -3
+    assert bwd(lib, lse=FAKE + 1) == -3
+    assert bwd(lib, ws_bytes=64) == -4
+    assert bwd(lib, ws=None) == -4
+    assert bwd(lib, ws=FAKE + 8) == -3
+    # no queries: q, o, dout, lse, dq may be null (k, v, dk, dv are still needed)
+    assert bwd(lib, Nq=0, q=None, o=None, do=None, lse=None, dq=None, k=None) == -1
+    # no queries and no keys: nothing to do
+    assert bwd(lib, Nq=0, Nk=0, q=None, o=None, do=None, lse=None, dq=None, k=None, v=None, dk=None,
+               dv=None) == 0
+
+
+def test_bwd_workspace_size(lib):
+    """D_i rows (fp32, padded to 256 bytes), then the fp32 dQ accumulator."""
+    up = lambda x: -(-x // 256) * 256
+    for B, Hq, Nq, d in ((1, 4, 200, 128), (2, 3, 77, 64), (1, 1, 1, 64)):
+        rows = B * Hq * Nq
+        assert eta.attn_bwd_workspace_size(B, Hq, Nq, d) == up(rows * 4) + rows * d * 4
+    assert eta.attn_bwd_workspace_size(1, 4, 200, 96) == 0
+    assert eta.attn_bwd_workspace_size(0, 4, 200, 64) == 0
+
+
 def dec(lib, ws_bytes=None, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, o=FAKE, lse=FAKE, S=4, Hq=8, Hkv=2, d=128,
         bs=16, mb=64, nb=256, scale=0.1, ws=FAKE):
     if ws_bytes is None:
