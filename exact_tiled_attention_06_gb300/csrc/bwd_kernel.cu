@@ -20,13 +20,16 @@
 //
 // Main kernel roles (192 threads):
 //   warps 0-3  element-wise work, thread = TMEM lane: P^T and dS^T rows (lane = key),
-//              then the dQ partial (lane = query) and the final dK, dV (lane = key)
+//              then the dQ partial (lane = d for d = 128, lane = query for d = 64) and
+//              the final dK, dV (lane = key)
 //   warp  4    TMEM allocation and tcgen05 MMA issue (one thread)
 //   warp  5    TMA producer (one thread): K and V once, then Q and dO per query tile
+//              into two stages, so that the next tile loads while the current one is used
 // TMEM columns: [0,128) S^T, then P^T packed bf16 in [64,128); [128,256) dP^T, then dS^T
-// packed in [192,256); the dQ partial goes to the columns freed by the softmax, d in
-// [0,64) to [0,64) and d in [64,128) to [128,192), so that no MMA writes a column another
-// MMA of the same tile still reads; dV and dK accumulate in [256,256+d) and [256+d,256+2d).
+// packed in [192,256); the dQ partial goes to the columns freed by the softmax ([0,64) and
+// [128,192): dQ^T's query halves for d = 128, dQ's 64 columns for d = 64), so that no MMA
+// writes a column another MMA of the same tile still reads; dV and dK accumulate in
+// [256,256+d) and [256+d,256+2d).
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -52,24 +55,32 @@ struct BwdCfg {
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
     static constexpr int kKOff = 0;                     // K tile (resident)
     static constexpr int kVOff = kTileBytes;            // V tile (resident)
-    static constexpr int kQOff = 2 * kTileBytes;        // Q tile of the current query tile
-    static constexpr int kDOOff = 3 * kTileBytes;       // dO tile
-    static constexpr int kDSOff = 4 * kTileBytes;       // dS^T, bf16, MN-major operand (32 KB)
+    static constexpr int kQOff = 2 * kTileBytes;        // Q tile, stage s at + s * kStageStride
+    static constexpr int kDOOff = 3 * kTileBytes;       // dO tile, stage s at + s * kStageStride
+    static constexpr int kStageStride = 2 * kTileBytes; // two stages: the next query tile loads
+                                                        // while the current one is in use
+    static constexpr int kDSOff = 6 * kTileBytes;       // dS^T, bf16, MN-major operand (32 KB)
     // lse (log2 units) and D of the tile's queries, 128 + 128 fp32, two buffers
     static constexpr int kVecOff = kDSOff + 2 * kBoxBytes;
     static constexpr int kBarOff = kVecOff + 2 * 2 * BQ * 4;
-    static constexpr int kNumBars = 10;
+    static constexpr int kNumBars = 12;
     static constexpr int kHolderOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kHolderOff + 4;
     static constexpr int kUsedBytes = kAbortOff + 4;
-    // at least ~120 KB so that two blocks never share an SM (each takes all of TMEM)
-    static constexpr int kSmemBytes = (kUsedBytes + 1024) > 122880 ? (kUsedBytes + 1024) : 122880;
+    // Dynamic shared memory: the used bytes plus what is left for aligning the base to
+    // 1024 bytes, within the 227 KB a block may have; at least ~120 KB so that two
+    // blocks never share an SM (each takes all of TMEM). The kernel checks that the
+    // aligned layout fits before it touches anything.
+    static constexpr int kMaxDynSmem = 227 * 1024;
+    static constexpr int kPadded = (kUsedBytes + 1024) < kMaxDynSmem ? (kUsedBytes + 1024) : kMaxDynSmem;
+    static constexpr int kSmemBytes = kPadded > 122880 ? kPadded : 122880;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kSCol = 0, kPCol = 64, kDPCol = 128, kDSCol = 192;
     static constexpr uint32_t kDQCol0 = 0, kDQCol1 = 128;  // dQ partial, d in [0,64) and [64,128)
     static constexpr uint32_t kDVCol = 256, kDKCol = 256 + D;
-    static_assert(kUsedBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kUsedBytes <= kMaxDynSmem, "shared memory budget");
     static_assert(kDKCol + D <= kTmemCols, "TMEM budget");
+    static_assert(kDQCol1 + 64 <= kDSCol && kDQCol0 + 64 <= kPCol, "dQ columns overlap P^T or dS^T");
 };
 
 struct BwdParams {
@@ -176,21 +187,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     const uint32_t bar0 = sb + C::kBarOff;
     const uint32_t kv_full = bar0;             // K and V tiles landed
-    const uint32_t st_full = bar0 + 8u;        // Q and dO of the current query tile landed
-    const uint32_t st_empty = bar0 + 16u;      // every MMA reading Q and dO is done
-    const uint32_t sdp_full = bar0 + 24u;      // S^T and dP^T are in TMEM
-    const uint32_t p_ready = bar0 + 32u;       // P^T, dS^T written (TMEM and shared memory)
-    const uint32_t dq_full = bar0 + 40u;       // the dQ partial is in TMEM
-    const uint32_t dq_read = bar0 + 48u;       // the dQ partial has been read out
-    const uint32_t fin = bar0 + 56u;           // every MMA is done
-    const uint32_t vec_full = bar0 + 64u;      // two barriers: statistics buffer 0 / 1 written
+    const uint32_t st_full = bar0 + 8u;        // two barriers: Q and dO of stage 0 / 1 landed
+    const uint32_t st_empty = bar0 + 24u;      // two barriers: every MMA reading stage 0 / 1 done
+    const uint32_t sdp_full = bar0 + 40u;      // S^T and dP^T are in TMEM
+    const uint32_t p_ready = bar0 + 48u;       // P^T, dS^T written (TMEM and shared memory)
+    const uint32_t dq_full = bar0 + 56u;       // the dQ partial is in TMEM
+    const uint32_t dq_read = bar0 + 64u;       // the dQ partial has been read out
+    const uint32_t fin = bar0 + 72u;           // every MMA is done
+    const uint32_t vec_full = bar0 + 80u;      // two barriers: statistics buffer 0 / 1 written
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
+    // The 1024-byte aligned layout must fit in what was requested (uniform for the block).
+    if (static_cast<int>(smem - smem_raw) + C::kUsedBytes > C::kSmemBytes) {
+        if (threadIdx.x == 0) report_error(p.err, kDevErrBounds);
+        return;
+    }
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         mbar_init(st_full, 1);
+        mbar_init(st_full + 8u, 1);
         mbar_init(st_empty, 1);
+        mbar_init(st_empty + 8u, 1);
         mbar_init(sdp_full, 1);
         mbar_init(p_ready, 128);
         mbar_init(dq_full, 1);
@@ -223,30 +241,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(sK + x * C::kBoxBytes, &tm_k, kv_full, 64 * x, kt * BK, bk);
                 tma_load_3d(sV + x * C::kBoxBytes, &tm_v, kv_full, 64 * x, kt * BK, bk);
             }
-            int it = 0;
+            int it = 0;  // query tiles issued; tile t uses stage t % 2, its (t / 2)-th use
             for (int g = 0; g < p.G; ++g) {
                 const int hq = hkv * p.G + g;
                 for (int qt = qlo; qt < qhi; ++qt, ++it) {
-                    if (it > 0 && !mbar_wait(st_empty, (it - 1) & 1, abort_flag, p.err)) goto producer_done;
-                    mbar_arrive_expect_tx(st_full, 2 * C::kTileBytes);
+                    const int st = it & 1;
+                    const uint32_t full = st_full + 8u * st;
+                    if (it >= 2 && !mbar_wait(st_empty + 8u * st, ((it >> 1) - 1) & 1, abort_flag, p.err))
+                        goto producer_done;
+                    mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+                    const uint32_t so = st * C::kStageStride;
 #pragma unroll
                     for (int x = 0; x < C::kBoxes; ++x) {
-                        tma_load_3d(sQ + x * C::kBoxBytes, &tm_q, st_full, 64 * x, qt * BQ, b * p.Hq + hq);
-                        tma_load_3d(sDO + x * C::kBoxBytes, &tm_do, st_full, 64 * x, qt * BQ, b * p.Hq + hq);
+                        tma_load_3d(sQ + so + x * C::kBoxBytes, &tm_q, full, 64 * x, qt * BQ, b * p.Hq + hq);
+                        tma_load_3d(sDO + so + x * C::kBoxBytes, &tm_do, full, 64 * x, qt * BQ, b * p.Hq + hq);
                     }
                 }
             }
         producer_done:
-            // never leave while a copy into this block's shared memory is in flight
+            // never leave while a copy into this block's shared memory is in flight: wait
+            // for the last tile issued on each stage
             mbar_wait(kv_full, 0, nullptr, p.err);
-            if (it > 0) mbar_wait(st_full, (it - 1) & 1, nullptr, p.err);
+            for (int t = it >= 2 ? it - 2 : 0; t < it; ++t) mbar_wait(st_full + 8u * (t & 1), (t >> 1) & 1, nullptr, p.err);
         }
     } else if (warp == kMmaWarpB) {
         // ================================================================ MMA issue
         if (lane == 0 && n_it > 0) {
             constexpr uint32_t idesc_kq = idesc_bf16_f32(BK, BQ, false, false);  // S^T, dP^T
             constexpr uint32_t idesc_pd = idesc_bf16_f32(BK, D, false, true);    // dV, dK (A in TMEM)
-            constexpr uint32_t idesc_dq = idesc_bf16_f32(BQ, 64, true, true);    // dQ half (A MN-major)
+            // dQ: d = 128 computes dQ^T = K^T dS^T (lane = d, so that the accumulator adds are
+            // coalesced along d), one 64-query half at a time; d = 64 computes dQ = dS K
+            // (lane = query, N = 64).
+            constexpr uint32_t idesc_dq = D == 128 ? idesc_bf16_f32(D, 64, true, true) : idesc_bf16_f32(BQ, 64, true, true);
             // K-major descriptors (16-wide k steps inside 128-byte rows, a new box every 64)
             const uint64_t kd = smem_desc_sw128(sK, 16, 1024), vd = smem_desc_sw128(sV, 16, 1024);
             const uint64_t qd = smem_desc_sw128(sQ, 16, 1024), dod = smem_desc_sw128(sDO, 16, 1024);
@@ -258,19 +284,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t ds_mn = smem_desc_sw128(sDS, C::kBoxBytes, 1024);
             bool ok = mbar_wait(kv_full, 0, abort_flag, p.err);
             for (int it = 0; it < n_it && ok; ++it) {
-                if (!mbar_wait(st_full, it & 1, abort_flag, p.err)) break;
+                const int st = it & 1;
+                if (!mbar_wait(st_full + 8u * st, (it >> 1) & 1, abort_flag, p.err)) break;
                 if (it > 0 && !mbar_wait(dq_read, (it - 1) & 1, abort_flag, p.err)) break;
                 tc_fence_after();
+                const uint64_t so = static_cast<uint64_t>((st * C::kStageStride) >> 4);  // stage offset
                 // S^T = K Q^T and dP^T = V dO^T (keys x queries)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::kSCol, kd + off, qd + off, idesc_kq, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::kSCol, kd + off, qd + so + off, idesc_kq, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::kDPCol, vd + off, dod + off, idesc_kq, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::kDPCol, vd + off, dod + so + off, idesc_kq, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(sdp_full);
                 if (!mbar_wait(p_ready, it & 1, abort_flag, p.err)) break;
@@ -278,23 +306,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dV += P^T dO and dK += dS^T Q (A from TMEM, 16 queries = 8 columns per step)
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::kDVCol, tmem + C::kPCol + kk * 8, do_mn + static_cast<uint64_t>(kk * 128),
+                    mma_ts(tmem + C::kDVCol, tmem + C::kPCol + kk * 8, do_mn + so + static_cast<uint64_t>(kk * 128),
                            idesc_pd, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::kDKCol, tmem + C::kDSCol + kk * 8, q_mn + static_cast<uint64_t>(kk * 128),
+                    mma_ts(tmem + C::kDKCol, tmem + C::kDSCol + kk * 8, q_mn + so + static_cast<uint64_t>(kk * 128),
                            idesc_pd, (it > 0 || kk > 0) ? 1u : 0u);
-                // dQ partial = dS K (queries x d), one 64-wide half of d at a time, into
-                // columns that neither dV nor dK reads
+                tc_commit(st_empty + 8u * st);  // Q and dO of this stage are no longer read
+                // dQ partial, into columns that neither dV nor dK reads
+                if constexpr (D == 128) {
+                    // dQ^T (d x queries) = K^T dS^T: A = K MN-major, B = dS^T MN-major, one
+                    // 64-query half (one 16 KB block of the dS^T buffer) at a time
 #pragma unroll
-                for (int h = 0; h < C::kBoxes; ++h)
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_ss(tmem + (h == 0 ? C::kDQCol0 : C::kDQCol1), k_mn + static_cast<uint64_t>(kk * 128),
+                                   ds_mn + static_cast<uint64_t>((h * C::kBoxBytes) >> 4) +
+                                       static_cast<uint64_t>(kk * 128),
+                                   idesc_dq, kk > 0 ? 1u : 0u);
+                } else {
+                    // dQ (queries x d) = dS K: A = dS MN-major, B = K MN-major
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_ss(tmem + (h == 0 ? C::kDQCol0 : C::kDQCol1), ds_mn + static_cast<uint64_t>(kk * 128),
-                               k_mn + static_cast<uint64_t>((h * C::kBoxBytes) >> 4) + static_cast<uint64_t>(kk * 128),
-                               idesc_dq, kk > 0 ? 1u : 0u);
+                        mma_ss(tmem + C::kDQCol0, ds_mn + static_cast<uint64_t>(kk * 128),
+                               k_mn + static_cast<uint64_t>(kk * 128), idesc_dq, kk > 0 ? 1u : 0u);
+                }
                 tc_commit(dq_full);
-                tc_commit(st_empty);
             }
             tc_commit(fin);
             mbar_wait(fin, 0, nullptr, p.err);
@@ -401,20 +439,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(p_ready);
-                // ---- the dQ partial (lane = query): add it to the fp32 accumulator
+                // ---- the dQ partial: add it to the fp32 accumulator
                 if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                {
-                    const long long q = q0 + row;
-                    float* dst = p.dq_acc + (rowbase + q) * D;
+                if constexpr (D == 128) {
+                    // dQ^T: lane = d (this thread's row), column = query. For each query the
+                    // 32 lanes of a warp add 32 consecutive floats: one 128-byte line.
+                    float* dst = p.dq_acc + (rowbase + q0) * D + row;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < BQ; c0 += 32) {
                         uint32_t r[32];
                         __syncwarp();
                         tmem_ld32(tmem + lane_base + (c0 < 64 ? C::kDQCol0 + c0 : C::kDQCol1 + (c0 - 64)), r);
+                        tmem_ld_wait_dep32(r);
+                        const int n_valid = static_cast<int>(min(32ll, static_cast<long long>(p.Nq) - (q0 + c0)));
+#pragma unroll
+                        for (int m = 0; m < 32; ++m)
+                            if (m < n_valid)
+                                asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + static_cast<long long>(c0 + m) * D),
+                                             "f"(__uint_as_float(r[m]))
+                                             : "memory");
+                    }
+                } else {
+                    // dQ: lane = query (this thread's row), column = d
+                    const long long q = q0 + row;
+                    float* dst = p.dq_acc + (rowbase + q) * D;
+                    uint32_t r[32];
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        __syncwarp();
+                        tmem_ld32(tmem + lane_base + C::kDQCol0 + c0, r);
                         tmem_ld_wait_dep32(r);
                         if (q < p.Nq) {
 #pragma unroll
