@@ -14,22 +14,31 @@
 // Three launches:
 //   attn_bwd_prep      D_i = rowsum(dO o O) in fp32, and a zeroed fp32 dQ accumulator
 //   attn_bwd_sm103     one CTA per (128-key tile, kv head): dK, dV accumulate in TMEM
-//                      over every query head of the group and every query tile that sees
-//                      the keys; each tile's dQ partial is added to the fp32 accumulator
+//                      over every query head of the group and every 64-query step that
+//                      sees the keys; each step's dQ partial is added to the accumulator
 //   attn_bwd_dq_out    dQ = scale * accumulator, rounded to bf16
 //
-// Main kernel roles (192 threads):
-//   warps 0-3  element-wise work, thread = TMEM lane: P^T and dS^T rows (lane = key),
-//              then the dQ partial (lane = d for d = 128, lane = query for d = 64) and
-//              the final dK, dV (lane = key)
-//   warp  4    TMEM allocation and tcgen05 MMA issue (one thread)
-//   warp  5    TMA producer (one thread): K and V once, then Q and dO per query tile
-//              into two stages, so that the next tile loads while the current one is used
-// TMEM columns: [0,128) S^T, then P^T packed bf16 in [64,128); [128,256) dP^T, then dS^T
-// packed in [192,256); the dQ partial goes to the columns freed by the softmax ([0,64) and
-// [128,192): dQ^T's query halves for d = 128, dQ's 64 columns for d = 64), so that no MMA
-// writes a column another MMA of the same tile still reads; dV and dK accumulate in
-// [256,256+d) and [256+d,256+2d).
+// Main kernel, per 64-query step j (keys are the TMEM lanes of every product but dQ^T):
+//   S^T  = K Q^T        (128 x 64)        dP^T = V dO^T       (128 x 64)
+//   P^T, dS^T           element-wise, written back to TMEM as bf16 (A operands), dS^T
+//                       also to shared memory (B operand of dQ^T)
+//   dV  += P^T dO       dK += dS^T Q      dQ^T = K^T dS^T     (d x 64, lane = d)
+// Roles (448 threads):
+//   warps 0-7   softmax: warp w owns TMEM lane quadrant w % 4 (32 keys) and the query
+//               group w / 4 (queries [32 g, 32 g + 32) of the step)
+//   warps 8-11  dQ readout: copy the step's dQ^T tile (lane = d) from TMEM to registers,
+//               release it, then add it to the fp32 accumulator; each warp instruction
+//               covers 32 consecutive d of one query (one 128-byte line)
+//   warp  12    TMEM allocation and tcgen05 MMA issue (one thread)
+//   warp  13    TMA producer (one thread): K and V once, Q and dO per step (3 stages)
+// TMEM columns: two step buffers (step j uses buffer j % 2, 128 columns at 128 (j % 2)):
+// S^T in its first 64 columns, dP^T in the last 64. The softmax packs P^T and dS^T (bf16)
+// into the S^T half (query group g: P^T at 32 g, dS^T at 32 g + 16), and dQ^T then lands
+// in the dP^T half. dV and dK accumulate in [256, 256 + d) and [256 + d, 256 + 2 d).
+// The MMA thread issues S^T and dP^T of step j + 1 before the gradient products of step
+// j, so that each step's softmax overlaps the tensor work of its neighbours.
+// For d = 64 the dQ^T product still has M = 128: rows 64..127 of its A operand point at
+// a zero-filled block of shared memory, and the readout skips those lanes.
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -41,46 +50,62 @@
 namespace attn {
 namespace {
 
-constexpr int BQ = 128;  // query rows per tile
-constexpr int BK = 128;  // keys per tile (TMEM lanes in the key-major products)
-constexpr int kBwdThreads = 192;
-constexpr int kMmaWarpB = 4;
-constexpr int kLoadWarpB = 5;
+constexpr int BQ = 64;   // queries per step
+constexpr int BK = 128;  // keys per CTA (TMEM lanes of S^T, dP^T, dV, dK)
+constexpr int kSoftmaxThreads = 256;  // warps 0-7
+constexpr int kReadoutWarp0 = 8;      // warps 8-11
+constexpr int kMmaWarpB = 12;
+constexpr int kLoadWarpB = 13;
+constexpr int kBwdThreads = 14 * 32;
+constexpr int kStagesB = 3;           // Q / dO stages
 constexpr float kLog2eB = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
-    static constexpr int kBoxes = D / 64;
-    static constexpr int kBoxBytes = 128 * 128;         // 128 rows x 128 bytes
-    static constexpr int kTileBytes = kBoxes * kBoxBytes;
+    static constexpr int kBoxes = D / 64;               // 64-column (128-byte) boxes
+    static constexpr int kKBox = BK * 128;              // one box of the K or V tile: 16 KB
+    static constexpr int kKVTile = kBoxes * kKBox;
+    static constexpr int kQBox = BQ * 128;              // one box of a Q or dO step tile: 8 KB
+    static constexpr int kQTile = kBoxes * kQBox;
     static constexpr int kKOff = 0;                     // K tile (resident)
-    static constexpr int kVOff = kTileBytes;            // V tile (resident)
-    static constexpr int kQOff = 2 * kTileBytes;        // Q tile, stage s at + s * kStageStride
-    static constexpr int kDOOff = 3 * kTileBytes;       // dO tile, stage s at + s * kStageStride
-    static constexpr int kStageStride = 2 * kTileBytes; // two stages: the next query tile loads
-                                                        // while the current one is in use
-    static constexpr int kDSOff = 6 * kTileBytes;       // dS^T, bf16, MN-major operand (32 KB)
-    // lse (log2 units) and D of the tile's queries, 128 + 128 fp32, two buffers
-    static constexpr int kVecOff = kDSOff + 2 * kBoxBytes;
+    static constexpr int kVOff = kKVTile;               // V tile (resident)
+    static constexpr int kZOff = 2 * kKVTile;           // d = 64: zeros standing in for d 64..127
+    static constexpr int kZBytes = D == 64 ? kKBox : 0;
+    static constexpr int kStageOff = kZOff + kZBytes;   // stage s: Q at + s * kStageBytes, dO after Q
+    static constexpr int kStageBytes = 2 * kQTile;
+    static constexpr int kDSOff = kStageOff + kStagesB * kStageBytes;  // dS^T, two buffers
+    static constexpr int kDSBytes = BK * 128;           // 128 keys x 64 queries x bf16
+    static constexpr int kVecOff = kDSOff + 2 * kDSBytes;  // two buffers: lse * log2(e) [64], D [64]
     static constexpr int kBarOff = kVecOff + 2 * 2 * BQ * 4;
-    static constexpr int kNumBars = 12;
+    static constexpr int kNumBars = 20;
     static constexpr int kHolderOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kHolderOff + 4;
     static constexpr int kUsedBytes = kAbortOff + 4;
-    // Dynamic shared memory: the used bytes plus what is left for aligning the base to
-    // 1024 bytes, within the 227 KB a block may have; at least ~120 KB so that two
-    // blocks never share an SM (each takes all of TMEM). The kernel checks that the
-    // aligned layout fits before it touches anything.
-    static constexpr int kMaxDynSmem = 227 * 1024;
-    static constexpr int kPadded = (kUsedBytes + 1024) < kMaxDynSmem ? (kUsedBytes + 1024) : kMaxDynSmem;
-    static constexpr int kSmemBytes = kPadded > 122880 ? kPadded : 122880;
+    // Dynamic shared memory: what is used plus room to align the base to 1024 bytes;
+    // at least ~120 KB so that two blocks never share an SM (each takes all of TMEM).
+    static constexpr int kSmemBytes = (kUsedBytes + 1024) > 122880 ? (kUsedBytes + 1024) : 122880;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kSCol = 0, kPCol = 64, kDPCol = 128, kDSCol = 192;
-    static constexpr uint32_t kDQCol0 = 0, kDQCol1 = 128;  // dQ partial, d in [0,64) and [64,128)
+    static constexpr uint32_t kBufCols = 128;           // one step buffer
+    static constexpr uint32_t kDPHalf = 64;             // dP^T, then dQ^T, within a buffer
     static constexpr uint32_t kDVCol = 256, kDKCol = 256 + D;
-    static_assert(kUsedBytes <= kMaxDynSmem, "shared memory budget");
+    static_assert(kUsedBytes + 1024 <= 227 * 1024, "shared memory budget");
     static_assert(kDKCol + D <= kTmemCols, "TMEM budget");
-    static_assert(kDQCol1 + 64 <= kDSCol && kDQCol0 + 64 <= kPCol, "dQ columns overlap P^T or dS^T");
+    static_assert(kStageOff % 1024 == 0 && kDSOff % 1024 == 0 && kZOff % 1024 == 0,
+                  "swizzled tiles need 1024-byte alignment");
+};
+
+// Barrier slots (8 bytes each) from kBarOff.
+enum BwdBar : uint32_t {
+    kBarKV = 0,          // K and V landed
+    kBarStFull = 1,      // + s: stage s of Q and dO landed (3)
+    kBarStEmpty = 4,     // + s: every MMA reading stage s is done (3)
+    kBarSFull = 7,       // + b: S^T of buffer b in TMEM (2)
+    kBarDPFull = 9,      // + b: dP^T of buffer b in TMEM (2)
+    kBarPReady = 11,     // + b: P^T, dS^T of buffer b written, TMEM and shared (2; 256 arrivals)
+    kBarDQFull = 13,     // + b: dQ^T of buffer b in TMEM (2)
+    kBarDQRead = 15,     // + b: dQ^T of buffer b copied to registers (2; 128 arrivals)
+    kBarVec = 17,        // + u: statistics buffer u written (2; 256 arrivals)
+    kBarFin = 19,        // every MMA done
 };
 
 struct BwdParams {
@@ -98,9 +123,6 @@ struct BwdParams {
     unsigned* err;
 };
 
-// ---------------------------------------------------------------------------- prep
-// One warp per row: D_i = sum_c dO_ic O_ic (fp32), and the row of the dQ accumulator
-// set to zero.
 template <int D>
 __global__ void __launch_bounds__(256)
     attn_bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
@@ -175,7 +197,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // Block order: key tile outer, (batch, kv head) inner, so that under a causal mask the
-    // tiles that see the most query tiles (the first key tiles) are scheduled first.
+    // tiles that see the most query steps (the first key tiles) are scheduled first.
     const int n_bk = p.B * p.Hkv;
     const int kt = static_cast<int>(blockIdx.x) / n_bk;
     const int bk = static_cast<int>(blockIdx.x) % n_bk;  // batch * Hkv + kv head
@@ -183,41 +205,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int hkv = bk % p.Hkv;
     int qlo, qhi;
     query_tile_range(p, kt, qlo, qhi);
-    const int n_it = p.G * (qhi - qlo);  // (query head of the group, query tile) pairs
+    const int n_it = p.G * (qhi - qlo);  // steps: (query head of the group, 64-query tile)
 
     const uint32_t bar0 = sb + C::kBarOff;
-    const uint32_t kv_full = bar0;             // K and V tiles landed
-    const uint32_t st_full = bar0 + 8u;        // two barriers: Q and dO of stage 0 / 1 landed
-    const uint32_t st_empty = bar0 + 24u;      // two barriers: every MMA reading stage 0 / 1 done
-    const uint32_t sdp_full = bar0 + 40u;      // S^T and dP^T are in TMEM
-    const uint32_t p_ready = bar0 + 48u;       // P^T, dS^T written (TMEM and shared memory)
-    const uint32_t dq_full = bar0 + 56u;       // the dQ partial is in TMEM
-    const uint32_t dq_read = bar0 + 64u;       // the dQ partial has been read out
-    const uint32_t fin = bar0 + 72u;           // every MMA is done
-    const uint32_t vec_full = bar0 + 80u;      // two barriers: statistics buffer 0 / 1 written
+#define BWD_BAR(i) (bar0 + 8u * static_cast<uint32_t>(i))
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
-    // The 1024-byte aligned layout must fit in what was requested (uniform for the block).
-    if (static_cast<int>(smem - smem_raw) + C::kUsedBytes > C::kSmemBytes) {
-        if (threadIdx.x == 0) report_error(p.err, kDevErrBounds);
-        return;
-    }
     if (threadIdx.x == 0) {
-        mbar_init(kv_full, 1);
-        mbar_init(st_full, 1);
-        mbar_init(st_full + 8u, 1);
-        mbar_init(st_empty, 1);
-        mbar_init(st_empty + 8u, 1);
-        mbar_init(sdp_full, 1);
-        mbar_init(p_ready, 128);
-        mbar_init(dq_full, 1);
-        mbar_init(dq_read, 128);
-        mbar_init(fin, 1);
-        mbar_init(vec_full, 128);
-        mbar_init(vec_full + 8u, 128);
+        mbar_init(BWD_BAR(kBarKV), 1);
+        for (int s = 0; s < kStagesB; ++s) {
+            mbar_init(BWD_BAR(kBarStFull + s), 1);
+            mbar_init(BWD_BAR(kBarStEmpty + s), 1);
+        }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(BWD_BAR(kBarSFull + u), 1);
+            mbar_init(BWD_BAR(kBarDPFull + u), 1);
+            mbar_init(BWD_BAR(kBarPReady + u), kSoftmaxThreads);
+            mbar_init(BWD_BAR(kBarDQFull + u), 1);
+            mbar_init(BWD_BAR(kBarDQRead + u), 128);
+            mbar_init(BWD_BAR(kBarVec + u), kSoftmaxThreads);
+        }
+        mbar_init(BWD_BAR(kBarFin), 1);
         *abort_flag = 0;
         fence_mbar_init();
+    }
+    if constexpr (C::kZBytes > 0) {
+        // zeros read by the tensor cores as rows 64..127 of the dQ^T product's A operand
+        for (int i = threadIdx.x; i < C::kZBytes / 16; i += kBwdThreads)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sb + C::kZOff + 16 * i), "r"(0u)
+                         : "memory");
+        fence_proxy_async_smem();
     }
     if (warp == kMmaWarpB) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
@@ -227,306 +245,314 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const uint32_t sK = sb + C::kKOff, sV = sb + C::kVOff, sQ = sb + C::kQOff, sDO = sb + C::kDOOff;
-    const uint32_t sDS = sb + C::kDSOff;
+    const uint32_t sK = sb + C::kKOff, sV = sb + C::kVOff;
+    const uint32_t sStage = sb + C::kStageOff, sDS = sb + C::kDSOff;
 
     if (warp == kLoadWarpB) {
         // ================================================================ producer
         if (lane == 0 && n_it > 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_do);
-            mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+            mbar_arrive_expect_tx(BWD_BAR(kBarKV), 2 * C::kKVTile);
 #pragma unroll
             for (int x = 0; x < C::kBoxes; ++x) {
-                tma_load_3d(sK + x * C::kBoxBytes, &tm_k, kv_full, 64 * x, kt * BK, bk);
-                tma_load_3d(sV + x * C::kBoxBytes, &tm_v, kv_full, 64 * x, kt * BK, bk);
+                tma_load_3d(sK + x * C::kKBox, &tm_k, BWD_BAR(kBarKV), 64 * x, kt * BK, bk);
+                tma_load_3d(sV + x * C::kKBox, &tm_v, BWD_BAR(kBarKV), 64 * x, kt * BK, bk);
             }
-            int it = 0;  // query tiles issued; tile t uses stage t % 2, its (t / 2)-th use
-            for (int g = 0; g < p.G; ++g) {
-                const int hq = hkv * p.G + g;
+            int it = 0, s = 0, ph = 0;  // step it uses stage s = it % 3 for the (it / 3)-th time, ph = that & 1
+            for (int gq = 0; gq < p.G; ++gq) {
+                const int zq = b * p.Hq + hkv * p.G + gq;
                 for (int qt = qlo; qt < qhi; ++qt, ++it) {
-                    const int st = it & 1;
-                    const uint32_t full = st_full + 8u * st;
-                    if (it >= 2 && !mbar_wait(st_empty + 8u * st, ((it >> 1) - 1) & 1, abort_flag, p.err))
+                    // the previous use of this stage must be released (its ((it / 3) - 1)-th release)
+                    if (it >= kStagesB && !mbar_wait(BWD_BAR(kBarStEmpty + s), ph ^ 1, abort_flag, p.err))
                         goto producer_done;
-                    mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
-                    const uint32_t so = st * C::kStageStride;
+                    const uint32_t full = BWD_BAR(kBarStFull + s);
+                    mbar_arrive_expect_tx(full, 2 * C::kQTile);
+                    const uint32_t so = sStage + s * C::kStageBytes;
 #pragma unroll
                     for (int x = 0; x < C::kBoxes; ++x) {
-                        tma_load_3d(sQ + so + x * C::kBoxBytes, &tm_q, full, 64 * x, qt * BQ, b * p.Hq + hq);
-                        tma_load_3d(sDO + so + x * C::kBoxBytes, &tm_do, full, 64 * x, qt * BQ, b * p.Hq + hq);
+                        tma_load_3d(so + x * C::kQBox, &tm_q, full, 64 * x, qt * BQ, zq);
+                        tma_load_3d(so + C::kQTile + x * C::kQBox, &tm_do, full, 64 * x, qt * BQ, zq);
+                    }
+                    if (++s == kStagesB) {
+                        s = 0;
+                        ph ^= 1;
                     }
                 }
             }
         producer_done:
             // never leave while a copy into this block's shared memory is in flight: wait
-            // for the last tile issued on each stage
-            mbar_wait(kv_full, 0, nullptr, p.err);
-            for (int t = it >= 2 ? it - 2 : 0; t < it; ++t) mbar_wait(st_full + 8u * (t & 1), (t >> 1) & 1, nullptr, p.err);
+            // for K, V and for the last step issued on each stage
+            mbar_wait(BWD_BAR(kBarKV), 0, nullptr, p.err);
+            for (int t = it > kStagesB ? it - kStagesB : 0; t < it; ++t)
+                mbar_wait(BWD_BAR(kBarStFull + t % kStagesB), (t / kStagesB) & 1, nullptr, p.err);
         }
     } else if (warp == kMmaWarpB) {
         // ================================================================ MMA issue
         if (lane == 0 && n_it > 0) {
-            constexpr uint32_t idesc_kq = idesc_bf16_f32(BK, BQ, false, false);  // S^T, dP^T
-            constexpr uint32_t idesc_pd = idesc_bf16_f32(BK, D, false, true);    // dV, dK (A in TMEM)
-            // dQ: d = 128 computes dQ^T = K^T dS^T (lane = d, so that the accumulator adds are
-            // coalesced along d), one 64-query half at a time; d = 64 computes dQ = dS K
-            // (lane = query, N = 64).
-            constexpr uint32_t idesc_dq = D == 128 ? idesc_bf16_f32(D, 64, true, true) : idesc_bf16_f32(BQ, 64, true, true);
-            // K-major descriptors (16-wide k steps inside 128-byte rows, a new box every 64)
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BK, BQ, false, false);   // S^T, dP^T
+            constexpr uint32_t idesc_g = idesc_bf16_f32(BK, D, false, true);     // dV, dK (A in TMEM)
+            constexpr uint32_t idesc_q = idesc_bf16_f32(128, BQ, true, true);    // dQ^T (M = 128 d rows)
+            // K-major operands of S^T and dP^T: 16-column k steps inside 128-byte rows, a
+            // new box every 64 columns (16 KB apart in K / V, 8 KB apart in Q / dO)
             const uint64_t kd = smem_desc_sw128(sK, 16, 1024), vd = smem_desc_sw128(sV, 16, 1024);
-            const uint64_t qd = smem_desc_sw128(sQ, 16, 1024), dod = smem_desc_sw128(sDO, 16, 1024);
-            // MN-major descriptors (16 rows of the reduction dimension = 2048 bytes per step,
-            // the two 64-wide halves of the other dimension one box apart)
-            const uint64_t q_mn = smem_desc_sw128(sQ, C::kBoxBytes, 1024);
-            const uint64_t do_mn = smem_desc_sw128(sDO, C::kBoxBytes, 1024);
-            const uint64_t k_mn = smem_desc_sw128(sK, C::kBoxBytes, 1024);
-            const uint64_t ds_mn = smem_desc_sw128(sDS, C::kBoxBytes, 1024);
-            bool ok = mbar_wait(kv_full, 0, abort_flag, p.err);
-            for (int it = 0; it < n_it && ok; ++it) {
-                const int st = it & 1;
-                if (!mbar_wait(st_full + 8u * st, (it >> 1) & 1, abort_flag, p.err)) break;
-                if (it > 0 && !mbar_wait(dq_read, (it - 1) & 1, abort_flag, p.err)) break;
+            // MN-major operands: 16 rows of the reduction dimension (2048 bytes) per k step
+            const uint64_t k_mn = smem_desc_sw128(sK, D == 128 ? C::kKBox : C::kZOff - C::kKOff, 1024);
+            const uint64_t st_k = smem_desc_sw128(sStage, 16, 1024);         // stage 0, K-major
+            const uint64_t st_mn = smem_desc_sw128(sStage, C::kQBox, 1024);  // stage 0, MN-major
+            const uint64_t ds_mn = smem_desc_sw128(sDS, C::kDSBytes, 1024);  // dS^T buffer 0
+            bool ok = mbar_wait(BWD_BAR(kBarKV), 0, abort_flag, p.err);
+
+            // S^T and dP^T of step j into buffer j % 2
+            auto issue_sdp = [&](int j) -> bool {
+                const int s = j % kStagesB, bf = j & 1;
+                if (!mbar_wait(BWD_BAR(kBarStFull + s), (j / kStagesB) & 1, abort_flag, p.err)) return false;
+                // buffer bf last held step j - 2: its dQ^T was copied out (and, by the commit
+                // that preceded, every MMA of step j - 2 is complete)
+                if (j >= 2 && !mbar_wait(BWD_BAR(kBarDQRead + bf), ((j >> 1) - 1) & 1, abort_flag, p.err))
+                    return false;
                 tc_fence_after();
-                const uint64_t so = static_cast<uint64_t>((st * C::kStageStride) >> 4);  // stage offset
-                // S^T = K Q^T and dP^T = V dO^T (keys x queries)
+                const uint32_t dbuf = tmem + bf * C::kBufCols;
+                const uint64_t qd = st_k + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+                const uint64_t dod = qd + static_cast<uint64_t>(C::kQTile >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::kSCol, kd + off, qd + so + off, idesc_kq, kk > 0 ? 1u : 0u);
+                    const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4);
+                    const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4);
+                    mma_ss(dbuf, kd + oa, qd + ob, idesc_s, kk > 0 ? 1u : 0u);
                 }
+                tc_commit(BWD_BAR(kBarSFull + bf));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + C::kDPCol, vd + off, dod + so + off, idesc_kq, kk > 0 ? 1u : 0u);
+                    const uint64_t oa = static_cast<uint64_t>(((kk >> 2) * C::kKBox + (kk & 3) * 32) >> 4);
+                    const uint64_t ob = static_cast<uint64_t>(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4);
+                    mma_ss(dbuf + C::kDPHalf, vd + oa, dod + ob, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(sdp_full);
-                if (!mbar_wait(p_ready, it & 1, abort_flag, p.err)) break;
+                tc_commit(BWD_BAR(kBarDPFull + bf));
+                return true;
+            };
+            // dV, dK and dQ^T of step j
+            auto issue_grad = [&](int j) -> bool {
+                const int s = j % kStagesB, bf = j & 1;
+                if (!mbar_wait(BWD_BAR(kBarPReady + bf), (j >> 1) & 1, abort_flag, p.err)) return false;
                 tc_fence_after();
-                // dV += P^T dO and dK += dS^T Q (A from TMEM, 16 queries = 8 columns per step)
+                const uint32_t dbuf = tmem + bf * C::kBufCols;
+                const uint64_t qm = st_mn + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+                const uint64_t dom = qm + static_cast<uint64_t>(C::kQTile >> 4);
+                // 16 queries per k step: query group kk / 2, its P^T at 32 g, dS^T at 32 g + 16
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::kDVCol, tmem + C::kPCol + kk * 8, do_mn + so + static_cast<uint64_t>(kk * 128),
-                           idesc_pd, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::kDVCol, dbuf + 32 * (kk >> 1) + 8 * (kk & 1),
+                           dom + static_cast<uint64_t>(kk * 128), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + C::kDKCol, tmem + C::kDSCol + kk * 8, q_mn + so + static_cast<uint64_t>(kk * 128),
-                           idesc_pd, (it > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(st_empty + 8u * st);  // Q and dO of this stage are no longer read
-                // dQ partial, into columns that neither dV nor dK reads
-                if constexpr (D == 128) {
-                    // dQ^T (d x queries) = K^T dS^T: A = K MN-major, B = dS^T MN-major, one
-                    // 64-query half (one 16 KB block of the dS^T buffer) at a time
+                    mma_ts(tmem + C::kDKCol, dbuf + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                           qm + static_cast<uint64_t>(kk * 128), idesc_g, (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(BWD_BAR(kBarStEmpty + s));  // Q and dO of this stage are no longer read
+                const uint64_t dsd = ds_mn + static_cast<uint64_t>((bf * C::kDSBytes) >> 4);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_ss(tmem + (h == 0 ? C::kDQCol0 : C::kDQCol1), k_mn + static_cast<uint64_t>(kk * 128),
-                                   ds_mn + static_cast<uint64_t>((h * C::kBoxBytes) >> 4) +
-                                       static_cast<uint64_t>(kk * 128),
-                                   idesc_dq, kk > 0 ? 1u : 0u);
-                } else {
-                    // dQ (queries x d) = dS K: A = dS MN-major, B = K MN-major
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_ss(tmem + C::kDQCol0, ds_mn + static_cast<uint64_t>(kk * 128),
-                               k_mn + static_cast<uint64_t>(kk * 128), idesc_dq, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(dq_full);
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_ss(dbuf + C::kDPHalf, k_mn + static_cast<uint64_t>(kk * 128),
+                           dsd + static_cast<uint64_t>(kk * 128), idesc_q, kk > 0 ? 1u : 0u);
+                tc_commit(BWD_BAR(kBarDQFull + bf));
+                return true;
+            };
+
+            ok = ok && issue_sdp(0);
+            for (int j = 0; j < n_it && ok; ++j) {
+                if (j + 1 < n_it && !issue_sdp(j + 1)) break;
+                if (!issue_grad(j)) break;
             }
-            tc_commit(fin);
-            mbar_wait(fin, 0, nullptr, p.err);
+            tc_commit(BWD_BAR(kBarFin));
+            mbar_wait(BWD_BAR(kBarFin), 0, nullptr, p.err);
         }
-    } else {
-        // ================================================================ warps 0-3
-        const int row = threadIdx.x;                       // TMEM lane owned by this thread
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    } else if (warp < kReadoutWarp0) {
+        // ================================================================ softmax warps 0-7
+        const int tid = threadIdx.x;
+        const int qd = warp & 3;                  // TMEM lane quadrant
+        const int grp = warp >> 2;                // query group: queries [32 grp, 32 grp + 32)
+        const int krow = 32 * qd + lane;          // key row in the tile = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
         const long long delta = static_cast<long long>(p.Nk) - p.Nq;
-        // Queries allowed to see key j (the key of this thread in the S^T, dP^T products):
-        // i in [i_min, i_max]; causal j <= i + delta, window j >= i + delta - w.
-        const long long j = static_cast<long long>(kt) * BK + row;
+        // Queries allowed to see this thread's key j: i in [i_min, i_max] (causal:
+        // j <= i + delta; window w: j >= i + delta - w; inside the sequence).
+        const long long j = static_cast<long long>(kt) * BK + krow;
         long long i_min = 0, i_max = static_cast<long long>(p.Nq) - 1;
         if (p.causal && j - delta > i_min) i_min = j - delta;
         if (p.window >= 0 && j - delta + p.window < i_max) i_max = j - delta + p.window;
         if (j >= p.Nk) i_max = -1;
         bool ok = true;
         int it = 0;
-        for (int g = 0; g < p.G && ok; ++g) {
-            const int hq = hkv * p.G + g;
-            const long long rowbase = (static_cast<long long>(b) * p.Hq + hq) * p.Nq;
+        for (int gq = 0; gq < p.G && ok; ++gq) {
+            const long long rowbase = (static_cast<long long>(b) * p.Hq + hkv * p.G + gq) * p.Nq;
             for (int qt = qlo; qt < qhi; ++qt, ++it) {
-                // ---- per-query statistics of this tile, in buffer it % 2. Every thread
-                // finished reading that buffer (two tiles ago) before it arrived on p_ready
-                // of the previous tile, which this thread's dq_full wait has seen complete.
-                const int u = it & 1;
-                float* s_lse2 = reinterpret_cast<float*>(smem + C::kVecOff) + u * 2 * BQ;  // lse * log2(e)
-                float* s_dvec = s_lse2 + BQ;                                                // D
-                {
-                    const int q = qt * BQ + row;
+                const int bf = it & 1;                 // TMEM step buffer, statistics buffer
+                const uint32_t par = (it >> 1) & 1;    // phase parity of this buffer's barriers
+                const long long q0 = static_cast<long long>(qt) * BQ;
+                // ---- lse * log2(e) and D of the step's 64 queries. The buffer was last read
+                // two steps ago; every thread arrived on the previous step's barrier after
+                // that read, and this thread has passed that barrier.
+                float* vec = reinterpret_cast<float*>(smem + C::kVecOff) + bf * 2 * BQ;
+                if (tid < BQ) {
+                    const long long q = q0 + tid;
                     float l2 = INFINITY, dd = 0.0f;
                     if (q < p.Nq) {
                         l2 = p.lse[rowbase + q] * kLog2eB;
                         dd = p.dvec[rowbase + q];
                     }
-                    s_lse2[row] = l2;
-                    s_dvec[row] = dd;
+                    vec[tid] = l2;
+                    vec[BQ + tid] = dd;
                 }
-                mbar_arrive(vec_full + 8u * u);
+                mbar_arrive(BWD_BAR(kBarVec + bf));
                 // (wait results are made warp-uniform: the tcgen05 loads and stores below are
                 // warp-collective and must be reached by all 32 lanes or by none)
-                if (!__all_sync(0xffffffffu, mbar_wait(vec_full + 8u * u, (it >> 1) & 1, abort_flag, p.err))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(BWD_BAR(kBarVec + bf), par, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
-                const long long q0 = static_cast<long long>(qt) * BQ;
-                const int c_lo = static_cast<int>(max(-1ll, min(static_cast<long long>(BQ), i_min - q0)));
-                const int c_hi = static_cast<int>(max(-1ll, min(static_cast<long long>(BQ), i_max - q0)));
-                const bool full = c_lo <= 0 && c_hi >= BQ - 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(sdp_full, it & 1, abort_flag, p.err))) {
+                const long long c0q = q0 + 32 * grp;  // first query of this group
+                const int c_lo = static_cast<int>(max(-1ll, min(32ll, i_min - c0q)));
+                const int c_hi = static_cast<int>(max(-1ll, min(32ll, i_max - c0q)));
+                const bool full = c_lo <= 0 && c_hi >= 31;
+                const float* l2v = vec + 32 * grp;
+                const float* ddv = vec + BQ + 32 * grp;
+                const uint32_t dbuf = tmem + lane_base + bf * C::kBufCols;
+                // ---- P^T = exp2(S^T * scale * log2e - lse * log2e), masked
+                if (!__all_sync(0xffffffffu, mbar_wait(BWD_BAR(kBarSFull + bf), par, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // ---- P^T and dS^T, 64 queries at a time (32 packed bf16 pairs per half).
-                // The upper half goes first: its packed rows land in columns whose fp32
-                // scores it has just read, and the lower half's packed rows land in
-                // columns the upper half has already consumed.
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int half = 1 - hh;
-                    uint32_t pp[32], pd[32];
+                uint32_t sr[32];
+                tmem_ld32(dbuf + 32 * grp, sr);
+                tmem_ld_wait_dep32(sr);
+                float pv[32];
 #pragma unroll
-                    for (int sub = 0; sub < 2; ++sub) {
-                        const int c0 = half * 64 + sub * 32;
-                        uint32_t sr[32], dr[32];
-                        tmem_ld32(tmem + lane_base + C::kSCol + c0, sr);
-                        tmem_ld32(tmem + lane_base + C::kDPCol + c0, dr);
-                        tmem_ld_wait_dep32(sr);
-                        tmem_ld_wait_dep32(dr);
+                for (int k = 0; k < 32; ++k) {
+                    const float pe = ex2_approx(fmaf(__uint_as_float(sr[k]), p.scale_log2, -l2v[k]));
+                    pv[k] = (full || (k >= c_lo && k <= c_hi)) ? pe : 0.0f;
+                }
+                // ---- dS^T = P^T (dP^T - D)
+                if (!__all_sync(0xffffffffu, mbar_wait(BWD_BAR(kBarDPFull + bf), par, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t dr[32];
+                tmem_ld32(dbuf + C::kDPHalf + 32 * grp, dr);
+                tmem_ld_wait_dep32(dr);
+                uint32_t pp[16], pd[16];
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2) {
-                            float pv[2], dv[2];
+                for (int k = 0; k < 32; k += 2) {
+                    const float d0 = pv[k] * (__uint_as_float(dr[k]) - ddv[k]);
+                    const float d1 = pv[k + 1] * (__uint_as_float(dr[k + 1]) - ddv[k + 1]);
+                    pp[k / 2] = pack_bf16x2(pv[k], pv[k + 1]);
+                    pd[k / 2] = pack_bf16x2(d0, d1);
+                }
+                // P^T and dS^T into the columns this group has just read (A operands of dV, dK)
+                tmem_st16(dbuf + 32 * grp, pp);
+                tmem_st16(dbuf + 32 * grp + 16, pd);
+                // dS^T into shared memory, the MN-major B operand of dQ^T: key krow is a
+                // 128-byte row of 64 queries, this group's 32 queries are its 16-byte chunks
+                // 4 grp .. 4 grp + 3, XOR-swizzled with (krow mod 8)
+                const uint32_t rbase = sDS + bf * C::kDSBytes + krow * 128;
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int c = c0 + k + e;
-                                const float pe =
-                                    ex2_approx(fmaf(__uint_as_float(sr[k + e]), p.scale_log2, -s_lse2[c]));
-                                const float de = pe * (__uint_as_float(dr[k + e]) - s_dvec[c]);
-                                const bool allowed = full || (c >= c_lo && c <= c_hi);
-                                pv[e] = allowed ? pe : 0.0f;
-                                dv[e] = allowed ? de : 0.0f;
-                            }
-                            pp[sub * 16 + k / 2] = pack_bf16x2(pv[0], pv[1]);
-                            pd[sub * 16 + k / 2] = pack_bf16x2(dv[0], dv[1]);
-                        }
-                    }
-                    // P^T and dS^T rows into TMEM (A operands of dV and dK) ...
-                    tmem_st32(tmem + lane_base + C::kPCol + half * 32, pp);
-                    tmem_st32(tmem + lane_base + C::kDSCol + half * 32, pd);
-                    // ... and dS^T into shared memory as the MN-major A operand of dQ:
-                    // queries [64 half, 64 half + 64) form one 16 KB block, key `row` is a
-                    // 128-byte row, its 16-byte chunks XOR-swizzled with (row mod 8).
-                    const uint32_t rbase = sDS + half * C::kBoxBytes + row * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint32_t addr = rbase + ((cc ^ (row & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pd[4 * cc]),
-                                     "r"(pd[4 * cc + 1]), "r"(pd[4 * cc + 2]), "r"(pd[4 * cc + 3])
-                                     : "memory");
-                    }
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint32_t addr = rbase + (((4 * grp + cc) ^ (krow & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pd[4 * cc]),
+                                 "r"(pd[4 * cc + 1]), "r"(pd[4 * cc + 2]), "r"(pd[4 * cc + 3])
+                                 : "memory");
                 }
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(p_ready);
-                // ---- the dQ partial: add it to the fp32 accumulator
-                if (!__all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, abort_flag, p.err))) {
+                mbar_arrive(BWD_BAR(kBarPReady + bf));
+            }
+        }
+        // ---- epilogue once every MMA is done: warps 0-3 write dV, warps 4-7 write dK
+        // (lane = key). Every lane loads (the TMEM loads are warp-collective); only lanes
+        // with a key inside the sequence store.
+        const bool have = n_it > 0 ? mbar_wait(BWD_BAR(kBarFin), 0, nullptr, p.err) : true;
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, have && ok && *abort_flag == 0)) {
+            const long long obase = ((static_cast<long long>(b) * p.Hkv + hkv) * p.Nk + j) * D;
+            __nv_bfloat16* out = grp == 0 ? p.dv : p.dk;
+            const float mul = grp == 0 ? 1.0f : p.scale;
+            const uint32_t col = grp == 0 ? C::kDVCol : C::kDKCol;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                __syncwarp();
+                if (n_it > 0) {
+                    tmem_ld32(tmem + lane_base + col + c0, r);
+                    tmem_ld_wait_dep32(r);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) r[k] = 0u;
+                }
+                if (j < p.Nk) {
+                    uint4* dst = reinterpret_cast<uint4*>(out + obase + c0);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[8 * m + 0]) * mul, __uint_as_float(r[8 * m + 1]) * mul);
+                        w.y = pack_bf16x2(__uint_as_float(r[8 * m + 2]) * mul, __uint_as_float(r[8 * m + 3]) * mul);
+                        w.z = pack_bf16x2(__uint_as_float(r[8 * m + 4]) * mul, __uint_as_float(r[8 * m + 5]) * mul);
+                        w.w = pack_bf16x2(__uint_as_float(r[8 * m + 6]) * mul, __uint_as_float(r[8 * m + 7]) * mul);
+                        dst[m] = w;
+                    }
+                }
+            }
+        }
+    } else {
+        // ================================================================ dQ readout warps 8-11
+        const int qd = warp & 3;                  // TMEM lane quadrant = d rows [32 qd, 32 qd + 32)
+        const int drow = 32 * qd + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+        const bool active = 32 * qd < D;          // d = 64: lanes 64..127 hold the zero padding
+        int it = 0;
+        bool ok = true;
+        for (int gq = 0; gq < p.G && ok; ++gq) {
+            const long long rowbase = (static_cast<long long>(b) * p.Hq + hkv * p.G + gq) * p.Nq;
+            for (int qt = qlo; qt < qhi; ++qt, ++it) {
+                const int bf = it & 1;
+                const uint32_t par = (it >> 1) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(BWD_BAR(kBarDQFull + bf), par, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if constexpr (D == 128) {
-                    // dQ^T: lane = d (this thread's row), column = query. For each query the
-                    // 32 lanes of a warp add 32 consecutive floats: one 128-byte line.
-                    float* dst = p.dq_acc + (rowbase + q0) * D + row;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < BQ; c0 += 32) {
-                        uint32_t r[32];
-                        __syncwarp();
-                        tmem_ld32(tmem + lane_base + (c0 < 64 ? C::kDQCol0 + c0 : C::kDQCol1 + (c0 - 64)), r);
-                        tmem_ld_wait_dep32(r);
-                        const int n_valid = static_cast<int>(min(32ll, static_cast<long long>(p.Nq) - (q0 + c0)));
-#pragma unroll
-                        for (int m = 0; m < 32; ++m)
-                            if (m < n_valid)
-                                asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + static_cast<long long>(c0 + m) * D),
-                                             "f"(__uint_as_float(r[m]))
-                                             : "memory");
-                    }
-                } else {
-                    // dQ: lane = query (this thread's row), column = d
-                    const long long q = q0 + row;
-                    float* dst = p.dq_acc + (rowbase + q) * D;
-                    uint32_t r[32];
-#pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        __syncwarp();
-                        tmem_ld32(tmem + lane_base + C::kDQCol0 + c0, r);
-                        tmem_ld_wait_dep32(r);
-                        if (q < p.Nq) {
-#pragma unroll
-                            for (int m = 0; m < 8; ++m)
-                                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c0 + 4 * m),
-                                             "f"(__uint_as_float(r[4 * m])), "f"(__uint_as_float(r[4 * m + 1])),
-                                             "f"(__uint_as_float(r[4 * m + 2])), "f"(__uint_as_float(r[4 * m + 3]))
-                                             : "memory");
-                        }
-                    }
-                }
+                const uint32_t src = tmem + lane_base + bf * C::kBufCols + C::kDPHalf;
+                uint32_t r[64];
+                tmem_ld32(src, r);
+                tmem_ld32(src + 32, r + 32);
+                tmem_ld_wait_dep32(r);
+                tmem_ld_wait_dep32(r + 32);
                 tc_fence_before();
-                mbar_arrive(dq_read);
-            }
-        }
-        // ---- dK, dV (lane = key) once every MMA is done. Every lane loads (the TMEM
-        // loads are warp-collective); only lanes with a key inside the sequence store.
-        const bool have = n_it > 0 ? mbar_wait(fin, 0, nullptr, p.err) : true;
-        tc_fence_after();
-        if (__all_sync(0xffffffffu, have && ok && *abort_flag == 0)) {
-            const long long obase = ((static_cast<long long>(b) * p.Hkv + hkv) * p.Nk + j) * D;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t rv[32], rk[32];
-                __syncwarp();
-                if (n_it > 0) {
-                    tmem_ld32(tmem + lane_base + C::kDVCol + c0, rv);
-                    tmem_ld32(tmem + lane_base + C::kDKCol + c0, rk);
-                    tmem_ld_wait_dep32(rv);
-                    tmem_ld_wait_dep32(rk);
-                } else {
+                mbar_arrive(BWD_BAR(kBarDQRead + bf));  // the TMEM buffer may be reused
+                if (active) {
+                    const long long q0 = static_cast<long long>(qt) * BQ;
+                    const int n_valid = static_cast<int>(min(static_cast<long long>(BQ), p.Nq - q0));
+                    float* dst = p.dq_acc + (rowbase + q0) * D + drow;
+                    if (n_valid == BQ) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) rv[k] = rk[k] = 0u;
-                }
-                if (j < p.Nk) {
-                    uint4* pv = reinterpret_cast<uint4*>(p.dv + obase + c0);
-                    uint4* pk = reinterpret_cast<uint4*>(p.dk + obase + c0);
+                        for (int m = 0; m < BQ; ++m) {
+                            asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(__uint_as_float(r[m])) : "memory");
+                            dst += D;
+                        }
+                    } else {
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        uint4 wv, wk;
-                        wv.x = pack_bf16x2(__uint_as_float(rv[8 * m + 0]), __uint_as_float(rv[8 * m + 1]));
-                        wv.y = pack_bf16x2(__uint_as_float(rv[8 * m + 2]), __uint_as_float(rv[8 * m + 3]));
-                        wv.z = pack_bf16x2(__uint_as_float(rv[8 * m + 4]), __uint_as_float(rv[8 * m + 5]));
-                        wv.w = pack_bf16x2(__uint_as_float(rv[8 * m + 6]), __uint_as_float(rv[8 * m + 7]));
-                        wk.x = pack_bf16x2(__uint_as_float(rk[8 * m + 0]) * p.scale, __uint_as_float(rk[8 * m + 1]) * p.scale);
-                        wk.y = pack_bf16x2(__uint_as_float(rk[8 * m + 2]) * p.scale, __uint_as_float(rk[8 * m + 3]) * p.scale);
-                        wk.z = pack_bf16x2(__uint_as_float(rk[8 * m + 4]) * p.scale, __uint_as_float(rk[8 * m + 5]) * p.scale);
-                        wk.w = pack_bf16x2(__uint_as_float(rk[8 * m + 6]) * p.scale, __uint_as_float(rk[8 * m + 7]) * p.scale);
-                        pv[m] = wv;
-                        pk[m] = wk;
+                        for (int m = 0; m < BQ; ++m) {
+                            if (m < n_valid)
+                                asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(__uint_as_float(r[m])) : "memory");
+                            dst += D;
+                        }
                     }
                 }
             }
         }
     }
+#undef BWD_BAR
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
@@ -563,8 +589,8 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
     if (grid > INT_MAX) return kErrInvalidArg;
     if (grid > 0) {
         CUtensorMap tq, tk, tv, tdo;
-        const uint32_t box[3] = {64u, 128u, 1u};
         {
+            const uint32_t box[3] = {64u, static_cast<uint32_t>(BK), 1u};
             const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nk),
                                       static_cast<uint64_t>(B) * Hkv};
             const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Nk) * D * 2};
@@ -574,6 +600,7 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
             if (rc != kOk) return rc;
         }
         if (Nq > 0) {
+            const uint32_t box[3] = {64u, static_cast<uint32_t>(BQ), 1u};
             const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nq),
                                       static_cast<uint64_t>(B) * Hq};
             const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(Nq) * D * 2};
