@@ -65,8 +65,10 @@ unsigned* device_error_word()
     return g_err_ptr[dev];
 }
 
-int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                    const uint64_t* strides_bytes, const uint32_t* box)
+namespace {
+
+int encode_map(CUtensorMap* map, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle, const void* base, int rank,
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box)
 {
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -91,11 +93,26 @@ int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t
         estride[i] = 1;
         if (i + 1 < rank) gstride[i] = strides_bytes[i];
     }
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
-                                const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gdim, gstride, bdim,
+                                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? kOk : kErrCuda;
+}
+
+}  // namespace
+
+int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box)
+{
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, rank, dims,
+                      strides_bytes, box);
+}
+
+int encode_f32_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                   const uint32_t* box)
+{
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, base, rank, dims,
+                      strides_bytes, box);
 }
 
 }  // namespace attn

@@ -28,6 +28,11 @@ enum : int {
 int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box);
 
+// Encode a tiled TMA descriptor over an fp32 tensor without swizzle (a box is stored
+// densely, row after row); used as the target of TMA reductions.
+int encode_f32_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                   const uint32_t* box);
+
 // Device address of the library's error word on the current device (nullptr on failure).
 unsigned* device_error_word();
 
