@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)  // 14 warps: at most 128 regi
                 const uint32_t tp = it & 1;               // per-tile barrier parity
                 const int u = it & 1;                     // statistics buffer
                 const long long q0 = static_cast<long long>(qt) * BQ;
-                // ---- lse * log2(e) and D of the tile's 128 queries. The buffer was last read
+                // ---- -lse * log2(e) and -D of the tile's 128 queries. The buffer was last read
                 // two tiles ago; every thread arrived on the previous tile's barrier after
                 // that read, and this thread has passed that barrier.
                 float* vec = reinterpret_cast<float*>(smem + C::kVecOff) + u * 2 * BQ;
@@ -426,8 +426,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)  // 14 warps: at most 128 regi
                         l2 = p.lse[rowbase + q] * kLog2eB;
                         dd = p.dvec[rowbase + q];
                     }
-                    vec[tid] = l2;
-                    vec[BQ + tid] = dd;
+                    vec[tid] = -l2;
+                    vec[BQ + tid] = -dd;
                 }
                 mbar_arrive(BWD_BAR(kBarVec + u));
                 // (wait results are made warp-uniform: the tcgen05 loads and stores below are
@@ -440,31 +440,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)  // 14 warps: at most 128 regi
                 const int c_lo = static_cast<int>(max(-1ll, min(64ll, i_min - c0q)));
                 const int c_hi = static_cast<int>(max(-1ll, min(64ll, i_max - c0q)));
                 const bool full = c_lo <= 0 && c_hi >= 63;
-                const float* l2v = vec + 64 * hh;
-                const float* ddv = vec + BQ + 64 * hh;
+                const float* nl2v = vec + 64 * hh;      // -lse * log2(e) of this half's queries
+                const float* nddv = vec + BQ + 64 * hh;  // -D of this half's queries
+                // off the diagonal (and inside a window) every key of the warp sees every query
+                // of the half: no per-element mask
+                const bool all_full = __all_sync(0xffffffffu, full);
                 // ---- P^T = exp2(S^T * scale * log2e - lse * log2e), masked, into TMEM as bf16
                 if (!__all_sync(0xffffffffu, mbar_wait(BWD_BAR(kBarSFull), tp, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // (exponent and product in paired fp32: one instruction per two elements)
+                const uint64_t c2 = f2pack(p.scale_log2, p.scale_log2);
                 float pv[64];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t sr[32];
                     tmem_ld32(tS + 32 * c, sr);
                     tmem_ld_wait_dep32(sr);
-                    float l2[32];  // lse * log2(e) of these 32 queries, read here (not hoisted)
+                    float nl2[32];  // read here, not hoisted (keeps registers for the products)
 #pragma unroll
                     for (int k = 0; k < 32; k += 4)
                         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                     : "=f"(l2[k]), "=f"(l2[k + 1]), "=f"(l2[k + 2]), "=f"(l2[k + 3])
-                                     : "r"(smem_u32(l2v + 32 * c + k)));
+                                     : "=f"(nl2[k]), "=f"(nl2[k + 1]), "=f"(nl2[k + 2]), "=f"(nl2[k + 3])
+                                     : "r"(smem_u32(nl2v + 32 * c + k)));
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int q = 32 * c + k;
-                        const float pe = ex2_approx(fmaf(__uint_as_float(sr[k]), p.scale_log2, -l2[k]));
-                        pv[q] = (full || (q >= c_lo && q <= c_hi)) ? pe : 0.0f;
+                    for (int k = 0; k < 32; k += 2) {
+                        float x0, x1;
+                        f2unpack(f2fma(f2pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2,
+                                       f2pack(nl2[k], nl2[k + 1])),
+                                 x0, x1);
+                        pv[32 * c + k] = ex2_approx(x0);
+                        pv[32 * c + k + 1] = ex2_approx(x1);
+                    }
+                    if (!all_full) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int q = 32 * c + k;
+                            pv[q] = (q >= c_lo && q <= c_hi) ? pv[q] : 0.0f;
+                        }
                     }
                 }
                 {
@@ -492,17 +507,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)  // 14 warps: at most 128 regi
                         uint32_t dr[16];
                         tmem_ld16(tDP + 32 * c + 16 * e, dr);
                         tmem_ld_wait_dep16(dr);
-                        float dd[16];  // D of these 16 queries, read here (not hoisted)
+                        float ndd[16];  // -D of these 16 queries, read here (not hoisted)
 #pragma unroll
                         for (int k = 0; k < 16; k += 4)
                             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                         : "=f"(dd[k]), "=f"(dd[k + 1]), "=f"(dd[k + 2]), "=f"(dd[k + 3])
-                                         : "r"(smem_u32(ddv + 32 * c + 16 * e + k)));
+                                         : "=f"(ndd[k]), "=f"(ndd[k + 1]), "=f"(ndd[k + 2]), "=f"(ndd[k + 3])
+                                         : "r"(smem_u32(nddv + 32 * c + 16 * e + k)));
 #pragma unroll
                         for (int k = 0; k < 16; k += 2) {
                             const int q = 32 * c + 16 * e + k;
-                            const float d0 = pv[q] * (__uint_as_float(dr[k]) - dd[k]);
-                            const float d1 = pv[q + 1] * (__uint_as_float(dr[k + 1]) - dd[k + 1]);
+                            float d0, d1;
+                            f2unpack(f2mul(f2pack(pv[q], pv[q + 1]),
+                                           f2add(f2pack(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])),
+                                                 f2pack(ndd[k], ndd[k + 1]))),
+                                     d0, d1);
                             pd[8 * e + k / 2] = pack_bf16x2(d0, d1);
                         }
                     }

@@ -319,6 +319,13 @@ __device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b)
     return d;
 }
 
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c)
 {
     float d;
