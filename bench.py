@@ -8,7 +8,9 @@
 Prints ONE JSON line (rank 0). ``value`` is prefill TFLOP/s (algorithmic FLOPs:
 4 * d per allowed (query, key) pair, i.e. 4 N^2 d per head halved for causal);
 ``decode`` carries the decode KV-read GB/s. Both inputs exceed the 129 MB L2,
-so no flush is needed between steps.
+so no flush is needed between steps. ``backward`` times attn_bwd on the prefill
+workload in a loop of its own after the step (same warm-up and step counts;
+10 * d FLOPs per allowed pair); ``--no-backward`` skips it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -55,6 +57,13 @@ def attention_flops(B, Hq, Nq, Nk, d, causal=False, window=-1) -> int:
     """Algorithmic FLOPs: two matmuls (Q K^T and P V), 2 FLOPs per multiply-add, over the
     allowed pairs -- 4 N^2 d per head without a mask ("Attention kernels", FLOP count)."""
     return 4 * d * allowed_pairs(Nq, Nk, causal, window) * B * Hq
+
+
+def backward_flops(B, Hq, Nq, Nk, d, causal=False, window=-1) -> int:
+    """Algorithmic FLOPs of the backward with the scores recomputed: five matmuls over the
+    allowed pairs (S = Q K^T, dP = dO V^T, dV = P^T dO, dK = dS^T Q, dQ = dS K), i.e.
+    2.5 times the forward ("Modern attention kernels", "Backward pass recomputes scores")."""
+    return 10 * d * allowed_pairs(Nq, Nk, causal, window) * B * Hq
 
 
 def score_matrix_bytes(N: int, bytes_per_el: int = 2) -> int:
@@ -108,6 +117,7 @@ def load_peaks():
 KERNEL_SOURCES = {
     "attn_fwd_sm103": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_decode_sm103": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_bwd_sm103": ("bwd_kernel.cu", "ptx.cuh", "internal.h"),
 }
 
 
@@ -342,8 +352,50 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = [float(np.mean([e_ev[i][j][0].elapsed_time(e_ev[i][j][1]) for i in range(e2e_steps)]))
                   for j in range(len(parts))]
 
+    # ---- backward of the prefill workload, in a loop of its own: W untimed launches,
+    #      then K launches bracketed by CUDA events on the launching stream (inputs and
+    #      the fp32 dQ accumulator exceed L2, so no flush is needed)
+    bwd_ms = None
+    pre = next((p for p in parts if p.name == "prefill"), None)
+    if pre is not None and not args.no_backward:
+        do_d = inputs.grad_output(pc.B, pc.Hq, pc.Nq, pc.d, seed=pc.seed + rank).to(dev)
+        ws_b = torch.empty(eta.attn_bwd_workspace_size(pc.B, pc.Hq, pc.Nq, pc.d), dtype=torch.uint8, device=dev)
+        dq = torch.empty_like(pre.dev["q"])
+        dk = torch.empty_like(pre.dev["k"])
+        dv = torch.empty_like(pre.dev["v"])
+        pre.run(pre.dev)  # o and lse of these inputs
+
+        def run_bwd():
+            eta.attn_bwd(pre.dev["q"], pre.dev["k"], pre.dev["v"], o, do_d, lse, causal=pc.causal,
+                         window=pc.window, scale=pc.scale, workspace=ws_b, dq=dq, dk=dk, dv=dv)
+
+        for _ in range(args.warmup):
+            run_bwd()
+        torch.cuda.synchronize()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the backward warm-up: {eta.attn_status_string(err)}")
+        b_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for e0, e1 in b_ev:
+            e0.record(stream)
+            run_bwd()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the timed backward: {eta.attn_status_string(err)}")
+        bwd_ms = np.array([e0.elapsed_time(e1) for e0, e1 in b_ev])
+
     # ---- max over ranks
-    vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms, world, dev)
+    vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms +
+                      ([float(bwd_ms.mean())] if bwd_ms is not None else []), world, dev)
+    bwd_mean = vals[-1] if bwd_ms is not None else None
+    vals = vals[:-1] if bwd_ms is not None else vals
     total_ms, means, e2e_ms = vals[0], vals[1:1 + len(parts)], vals[1 + len(parts):]
     if rank != 0:
         return None
@@ -413,6 +465,22 @@ def run_ours(args, rank, world, local_rank):
         result["e2e"] = e2e
     result["gpu_launches"] = sum(p.launches for p in parts) * args.steps
     result["clocks"] = clocks.summary()
+    if bwd_ms is not None:
+        flops = backward_flops(pc.B, pc.Hq, pc.Nq, pc.Nk, pc.d, pc.causal, pc.window)
+        achieved = flops / (bwd_mean * 1e-3) / 1e12
+        result["backward"] = {
+            "value": round(whole_job_rate(flops, world, bwd_mean, 1e12), 2), "unit": "TFLOP/s",
+            "workload": f"attn_bwd on {pc.name}", "flops_per_launch": flops, "steps": args.steps,
+            "warmup": args.warmup, "gpu_launches": 3 * args.steps,
+            "roofline": {"kernel": "attn_bwd_prep + attn_bwd_sm103<128> + attn_bwd_dq_out", "bound": "tensor",
+                         "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "peak_kind": f"{peak_kind} bf16 dense burst",
+                         "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                         "traffic": load_traffic("attn_bwd_sm103"),
+                         "ms_per_launch": round(bwd_mean, 4),
+                         "ms_p10_p50_p90": [round(float(np.percentile(bwd_ms, x)), 4) for x in (10, 50, 90)]},
+        }
     return result
 
 
@@ -503,6 +571,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
     ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
                     help="profiling aid: run only one half of the step (the JSON line then omits the other)")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences than the workload's 64")
     args = ap.parse_args()

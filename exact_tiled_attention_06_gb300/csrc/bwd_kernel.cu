@@ -1,10 +1,11 @@
 // bwd_kernel.cu -- attention backward for sm_103a: dQ, dK, dV from Q, K, V, O, dO and
 // the forward's per-row lse, with the score tiles recomputed.
 //
-// Pages: "Modern attention kernels", "Backward pass recomputes scores" (the forward
-// saves compact per-row statistics; the backward recomputes score tiles instead of
-// storing P); "Flash attention and IO-aware attention" (save only the row statistics,
-// recompute P block by block); "Attention kernels" (recompute from Q, K, V on the fly).
+// Pages: "Modern attention kernels", "Backward pass recomputes scores" (storing P would
+// cost quadratic memory: a per-row statistic is kept and the score tiles are formed
+// again); "Flash attention and IO-aware attention", the backward-pass paragraph (two
+// numbers per row kept, probabilities rebuilt tile by tile); "Attention kernels", the
+// rematerialisation passage (extra FLOPs traded for memory traffic).
 //
 // For a row i and key j (P_ij = 2^(s_ij * scale * log2e - lse_i * log2e), 0 if masked):
 //   dV_j = sum_i P_ij dO_i          dP_ij = dO_i . v_j          D_i = dO_i . O_i

@@ -18,8 +18,9 @@
 //     lse. A sequence that fits in one chunk is written directly.
 //
 // Pages: "Modern attention kernels", "Prefill and decode need different kernels"
-// (coalesced cache reads, parallel reduction across the context, grouped-query
-// sharing, block indirection, many sequences per batch) and "Paged attention changes
+// (decode is memory-bound: wide contiguous cache reads, one query's context spread over
+// many blocks and combined, a kv head read once for its query heads, the block table
+// followed, many sequences in one launch) and "Paged attention changes
 // addressing" (logical block = pos / block_size, offset = pos % block_size, physical =
 // table[seq, block]); "Attention kernels", FlashDecoding (chunk partials O_c, m_c, l_c
 // merged with the online-softmax rescaling) and the GQA paragraph. Decode is

@@ -83,10 +83,11 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d);
  * attn_bwd -- gradients of attention: dQ, dK, dV of L = sum(dO o O) for the O that
  *   attn_fwd computes from the same q, k, v, scale, causal and window.
  *
- *   MAK "Backward pass recomputes scores" (the forward keeps only the per-row
- *   statistic; the backward recomputes score tiles from Q, K, V instead of reading a
- *   stored P); IOA (only the softmax row statistics are saved, P is recomputed block
- *   by block in the backward); AK (recomputation instead of materialising attention).
+ *   MAK "Backward pass recomputes scores" (keeping P for the backward would cost
+ *   quadratic memory, so only a per-row statistic is kept and the score tiles are
+ *   formed again); IOA, the backward-pass paragraph (two numbers per row kept, the
+ *   probabilities rebuilt tile by tile); AK, the rematerialisation passage (more FLOPs,
+ *   less memory traffic).
  *   With P_ij = exp(scale q_i.k_j - lse_i) (0 where masked):
  *     dV_j = sum_i P_ij dO_i,   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,
  *     dS_ij = P_ij (dP_ij - D_i),   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i.
@@ -128,9 +129,10 @@ size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int bloc
 /*
  * attn_decode -- one query token per sequence against a paged KV cache.
  *
- *   MAK "Prefill and decode need different kernels" (coalesced cache reads, parallel
- *   reduction across the context, grouped-query head sharing, cache block
- *   indirection); MAK "Paged attention changes addressing" (logical block =
+ *   MAK "Prefill and decode need different kernels" (decode is memory-bound: read the
+ *   cache in wide contiguous pieces, spread one query's context over many blocks and
+ *   combine their results, let a kv head serve all of its query heads, follow the
+ *   block table); MAK "Paged attention changes addressing" (logical block =
  *   pos / block_size, offset = pos % block_size, physical = block_table[seq, block],
  *   address = base + physical * block_stride + offset * token_stride);
  *   AK FlashDecoding (split-KV partials merged with the online-softmax rescaling);

@@ -266,7 +266,7 @@ int oracle_attn_fwd_blocked(const double* q, const double* k, const double* v, d
 /* ------------------------------------------------------------------------- */
 /* Split-KV variant with the two-partial merge.                                */
 /* [AK] FlashDecoding: the keys of a row are cut into chunks; each chunk gives */
-/*   a partial output O_c with its own max m_c and sum l_c; the partials are   */
+/*   a partial output O_c together with that chunk's m_c and l_c; these are   */
 /*   merged with the same rescaling:                                           */
 /*     m = max_c m_c,  l = sum_c l_c e^{m_c - m},                              */
 /*     O = sum_c O_c (l_c e^{m_c - m} / l).                                    */

@@ -44,3 +44,11 @@ def test_flops_per_head():
 
 def test_decode_bytes():
     assert bench.decode_kv_bytes([1024, 2048], 8, 128) == (1024 + 2048) * 8 * 128 * 2 * 2
+
+
+def test_backward_flops_are_five_matmuls():
+    """Backward: 5 matmuls of 2 d FLOPs per allowed pair, 2.5 x the forward's 2."""
+    for args in ((1, 32, 8192, 8192, 128, True, -1), (2, 32, 4096, 4096, 128, True, 1024), (1, 1, 7, 13, 64, False, -1)):
+        assert bench.backward_flops(*args) * 2 == bench.attention_flops(*args) * 5
+    # one head, no mask: 10 N^2 d
+    assert bench.backward_flops(1, 1, 64, 64, 128) == 10 * 64 * 64 * 128
