@@ -26,6 +26,9 @@ What each function follows (pages by title and section):
 * ``attn_decode`` -- one query per sequence over a paged cache, addressed with
   the block-table formula of "Modern attention kernels",
   "Paged attention changes addressing".
+* ``attn_prefill_paged`` -- several new queries per sequence over a paged cache
+  (chunked prefill): the keys are gathered with the same formula and each new row
+  goes through the materialised row routine, bottom-right causal.
 
 Pins: every function is checked in ``tests/test_oracle_pins.py`` against
 closed forms, invariants, brute force on tiny inputs and a hand-derived golden
@@ -77,9 +80,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attn_fwd_split.argtypes = [_D, _D, _D, _D, _D] + [c_int] * 6 + [c_double, c_int, c_int, c_int]
     lib.oracle_attn_decode.argtypes = [_D, _D, _D, _I32, _I32, _D, _D] + [c_int] * 7 + [c_double]
     lib.oracle_attn_bwd.argtypes = [_D] * 7 + [c_int] * 6 + [c_double, c_int, c_int]
+    lib.oracle_attn_prefill_paged.argtypes = [_D, _D, _D, _I32, _I32, _I32, _D, _D] + [c_int] * 8 + [c_double, c_int,
+                                                                                                   c_int]
     lib.oracle_num_threads.argtypes = []
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows, lib.oracle_attn_fwd_blocked,
-              lib.oracle_attn_fwd_split, lib.oracle_attn_decode, lib.oracle_attn_bwd, lib.oracle_num_threads):
+              lib.oracle_attn_fwd_split, lib.oracle_attn_decode, lib.oracle_attn_bwd, lib.oracle_attn_prefill_paged,
+              lib.oracle_num_threads):
         f.restype = c_int
     return lib
 
@@ -185,6 +191,26 @@ class Oracle:
                                         Nk, d, float(scale), int(bool(causal)), int(window)), "oracle_attn_bwd")
         return dq, dk, dv
 
+    def attn_prefill_paged(self, q, k_cache, v_cache, block_table, q_lens, kv_lens, scale, causal=True, window=-1):
+        """Paged prefill. q [S][Hq][max_q][d]; caches [num_blocks][Hkv][bs][d]; block_table int32
+        [S][max_blocks]; q_lens, kv_lens int32 [S]. Returns (o, lse) shaped like q and [S][Hq][max_q];
+        rows i >= q_lens[s] are zero in o and NaN in lse (not computed)."""
+        q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+        kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+        S, Hq, max_q, d = q.shape
+        nb, Hkv, bs, dk = kc.shape
+        if dk != d or vc.shape != kc.shape or bt.ndim != 2 or bt.shape[0] != S or ql.shape != (S,) or kl.shape != (S,):
+            raise ValueError("paged prefill shape mismatch")
+        o = np.zeros(q.shape)
+        lse = np.full((S, Hq, max_q), np.nan)
+        _check(self.lib.oracle_attn_prefill_paged(_p(q), _p(kc), _p(vc), bt.ctypes.data_as(_I32),
+                                                  ql.ctypes.data_as(_I32), kl.ctypes.data_as(_I32), _p(o), _p(lse),
+                                                  S, Hq, Hkv, d, bs, bt.shape[1], nb, max_q, float(scale),
+                                                  int(bool(causal)), int(window)), "oracle_attn_prefill_paged")
+        return o, lse
+
     def attn_decode(self, q, k_cache, v_cache, block_table, seq_lens, scale):
         """Paged one-query decode. q [S][Hq][d]; caches [num_blocks][Hkv][bs][d];
         block_table int32 [S][max_blocks]; seq_lens int32 [S]. Returns (o [S][Hq][d], lse [S][Hq])."""
@@ -236,6 +262,10 @@ def attn_decode(*a, **kw):
 
 def attn_bwd(*a, **kw):
     return default().attn_bwd(*a, **kw)
+
+
+def attn_prefill_paged(*a, **kw):
+    return default().attn_prefill_paged(*a, **kw)
 
 
 def num_threads() -> int:

@@ -419,6 +419,86 @@ int oracle_attn_decode(const double* q, const double* k_cache, const double* v_c
 }
 
 /* ------------------------------------------------------------------------- */
+/* Prefill of several sequences against a paged cache (chunked prefill).       */
+/* [MAK] "Paged attention changes addressing": token t of a sequence sits in   */
+/*   logical block t / block_size at offset t % block_size; the block table    */
+/*   gives the physical block, and the address is base + physical *            */
+/*   block_stride + offset * token_stride (the same formula as decode above).  */
+/* Reading for several new queries: sequence s holds kv_lens[s] tokens in the  */
+/*   cache, the last q_lens[s] of which are its new queries, so query row i    */
+/*   sits at position kv_len - q_len + i (the bottom-right causal alignment of */
+/*   the prefill functions, with Nq = q_len and Nk = kv_len).                  */
+/* Each (sequence, kv head) gathers its keys and values into contiguous rows   */
+/* with that formula and hands every new query row to the materialised row     */
+/* routine above. q, o: [S][Hq][max_q][d]; lse: [S][Hq][max_q]; rows i >=      */
+/* q_lens[s] are neither read nor written.                                     */
+/* ------------------------------------------------------------------------- */
+int oracle_attn_prefill_paged(const double* q, const double* k_cache, const double* v_cache,
+                              const int32_t* block_table, const int32_t* q_lens, const int32_t* kv_lens,
+                              double* o, double* lse,
+                              int num_seqs, int Hq, int Hkv, int d, int block_size,
+                              int max_blocks_per_seq, int num_blocks, int max_q,
+                              double scale, int causal, int window)
+{
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || block_size <= 0 || max_q < 0 ||
+        max_blocks_per_seq < 0 || num_blocks < 0 || Hq % Hkv != 0)
+        return ORACLE_EINVAL;
+    long max_kv = 0;
+    for (int sq = 0; sq < num_seqs; ++sq) {
+        long qn = q_lens[sq], kn = kv_lens[sq];
+        if (qn < 0 || qn > max_q || kn < qn || kn > (long)max_blocks_per_seq * block_size) return ORACLE_EINVAL;
+        for (long lb = 0; lb < (kn + block_size - 1) / block_size; ++lb) {
+            int32_t phys = block_table[(long)sq * max_blocks_per_seq + lb];
+            if (phys < 0 || phys >= num_blocks) return ORACLE_EBOUNDS;
+        }
+        if (kn > max_kv) max_kv = kn;
+    }
+    int G = Hq / Hkv;
+    long block_stride = (long)Hkv * block_size * d;
+    long token_stride = d;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        size_t n = (size_t)(max_kv > 0 ? max_kv : 1);
+        double* kh = (double*)malloc(sizeof(double) * n * (size_t)d);
+        double* vh = (double*)malloc(sizeof(double) * n * (size_t)d);
+        double* sr = (double*)malloc(sizeof(double) * n);
+        double* pr = (double*)malloc(sizeof(double) * n);
+        if (!kh || !vh || !sr || !pr) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 1) collapse(2)
+            for (long sq = 0; sq < num_seqs; ++sq) {
+                for (long h = 0; h < Hq; ++h) {
+                    long hk = h / G;
+                    long qn = q_lens[sq], kn = kv_lens[sq];
+                    for (long t = 0; t < kn; ++t) {
+                        long blk = t / block_size, off = t % block_size;
+                        long phys = block_table[sq * max_blocks_per_seq + blk];
+                        long addr = phys * block_stride + off * token_stride + hk * (long)block_size * d;
+                        for (int c = 0; c < d; ++c) {
+                            kh[t * d + c] = k_cache[addr + c];
+                            vh[t * d + c] = v_cache[addr + c];
+                        }
+                    }
+                    for (long i = 0; i < qn; ++i) {
+                        long row = (sq * Hq + h) * (long)max_q + i;
+                        attend_row_materialised(q + row * d, kh, vh, i, qn, kn, d, scale, causal, window,
+                                                sr, pr, o + row * d, lse + row);
+                    }
+                }
+            }
+        }
+        free(kh);
+        free(vh);
+        free(sr);
+        free(pr);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Backward pass, materialised.                                                */
 /* [MAK] "Backward pass recomputes scores" and [IOA] (backward paragraph): the  */
 /*   gradients are formed from the same scores; here every row's score and     */

@@ -395,6 +395,56 @@ def pin_bwd_gqa_equals_duplicated_heads(orc):
         _close(dv, dv2.reshape(1, 2, 3, Nk, 4).sum(axis=2), 1e-12, f"GQA dv mask{mi}")
 
 
+def _paged_case(seed, S, Hq, Hkv, d, bs, q_lens, kv_lens, max_q, identity=False, extra=2):
+    r = _rng(seed)
+    kv = np.asarray(kv_lens, dtype=np.int32)
+    nblk = (kv + bs - 1) // bs
+    mb = int(max(1, nblk.max()))
+    nb = int(nblk.sum()) + extra
+    perm = np.arange(nb) if identity else r.permutation(nb)
+    table = np.full((S, mb), -1, dtype=np.int32)
+    pos = 0
+    for s in range(S):
+        table[s, :nblk[s]] = perm[pos:pos + nblk[s]]
+        pos += nblk[s]
+    kc = r.standard_normal((nb, Hkv, bs, d))
+    vc = r.standard_normal((nb, Hkv, bs, d))
+    q = r.standard_normal((S, Hq, max_q, d))
+    return q, kc, vc, table, np.asarray(q_lens, dtype=np.int32), kv
+
+
+def pin_paged_prefill_single_query_is_decode(orc):
+    """One new query per sequence: the last position sees every key, as in decode."""
+    S, Hq, Hkv, d, bs = 4, 6, 2, 8, 4
+    kv = [1, 5, 9, 13]
+    q, kc, vc, table, ql, kl = _paged_case(1800, S, Hq, Hkv, d, bs, [1] * S, kv, 3)
+    o, lse = orc.attn_prefill_paged(q, kc, vc, table, ql, kl, 0.5, causal=True)
+    od, ld = orc.attn_decode(q[:, :, 0, :], kc, vc, table, kl, 0.5)
+    _close(o[:, :, 0, :], od, 1e-14, "paged prefill q_len=1 O")
+    _close(lse[:, :, 0], ld, 1e-14, "paged prefill q_len=1 lse")
+    assert np.all(o[:, :, 1:, :] == 0) and np.all(np.isnan(lse[:, :, 1:])), "rows past q_len must stay untouched"
+
+
+def pin_paged_prefill_equals_gathered_prefill(orc):
+    """Keys and values gathered with numpy fancy indexing (a second implementation of
+    the address formula), then the pinned prefill with Nq = q_len, Nk = kv_len."""
+    S, Hq, Hkv, d = 3, 4, 2, 8
+    for bs, identity in ((4, True), (4, False), (8, False), (16, False)):
+        for causal, window in ((True, -1), (False, -1), (True, 3)):
+            ql, kv = [5, 1, 7], [9, 1, 23]
+            q, kc, vc, table, ql, kl = _paged_case(1850 + bs + (7 if identity else 0), S, Hq, Hkv, d, bs, ql, kv, 8,
+                                                   identity=identity)
+            o, lse = orc.attn_prefill_paged(q, kc, vc, table, ql, kl, 0.3, causal=causal, window=window)
+            for s in range(S):
+                t = np.arange(kl[s])
+                phys = table[s, t // bs]
+                ks = kc[phys, :, t % bs, :].transpose(1, 0, 2)  # [Hkv][kv_len][d]
+                vs = vc[phys, :, t % bs, :].transpose(1, 0, 2)
+                of, lf = orc.attn_fwd(q[s:s + 1, :, :ql[s], :], ks[None], vs[None], 0.3, causal, window)
+                _close(o[s, :, :ql[s], :], of[0], 1e-14, f"paged prefill bs={bs} seq{s} O")
+                _close(lse[s, :, :ql[s]], lf[0], 1e-14, f"paged prefill bs={bs} seq{s} lse")
+
+
 ALL_PINS = [
     pin_blocked_equals_materialised,
     pin_split_equals_unsplit,
@@ -414,4 +464,6 @@ ALL_PINS = [
     pin_bwd_torch_autograd,
     pin_bwd_invariants,
     pin_bwd_gqa_equals_duplicated_heads,
+    pin_paged_prefill_single_query_is_decode,
+    pin_paged_prefill_equals_gathered_prefill,
 ]

@@ -32,6 +32,9 @@ MUTANTS = [
     ("bwd_dk_from_k", "dkj[t] += scale * ds * qi[t];", "dkj[t] += scale * ds * kj[t];"),
     ("bwd_dq_missing_scale", "dqi[t] += scale * ds * kj[t];", "dqi[t] += ds * kj[t];"),
     ("bwd_dv_from_dp", "dvj[t] += p[j] * doi[t];", "dvj[t] += dp[j] * doi[t];"),
+    ("paged_prefill_no_head_offset", "off * token_stride + hk * (long)block_size * d;", "off * token_stride;"),
+    ("paged_prefill_top_left_alignment", "kh, vh, i, qn, kn, d, scale", "kh, vh, i, kn, kn, d, scale"),
+    ("paged_prefill_offset_by_block", "off = t % block_size;", "off = t / block_size;"),
 ]
 
 
