@@ -10,7 +10,9 @@ Prints ONE JSON line (rank 0). ``value`` is prefill TFLOP/s (algorithmic FLOPs:
 ``decode`` carries the decode KV-read GB/s. Both inputs exceed the 129 MB L2,
 so no flush is needed between steps. ``backward`` times attn_bwd on the prefill
 workload in a loop of its own after the step (same warm-up and step counts;
-10 * d FLOPs per allowed pair); ``--no-backward`` skips it.
+10 * d FLOPs per allowed pair); ``--no-backward`` skips it. ``paged_prefill`` times
+attn_prefill_paged on the chunked-prefill workload (16 sequences, 2048 new queries
+each over a paged cache) the same way; ``--no-paged-prefill`` skips it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -66,6 +68,12 @@ def backward_flops(B, Hq, Nq, Nk, d, causal=False, window=-1) -> int:
     return 10 * d * allowed_pairs(Nq, Nk, causal, window) * B * Hq
 
 
+def paged_prefill_flops(q_lens, kv_lens, Hq, d, causal=True, window=-1) -> int:
+    """Algorithmic FLOPs of prefill over a paged cache: 4 d per allowed pair, each sequence
+    with its own Nq = q_len and Nk = kv_len (bottom-right alignment)."""
+    return int(sum(4 * d * allowed_pairs(int(a), int(b), causal, window) * Hq for a, b in zip(q_lens, kv_lens)))
+
+
 def score_matrix_bytes(N: int, bytes_per_el: int = 2) -> int:
     """Size of one head's N x N score matrix."""
     return N * N * bytes_per_el
@@ -118,6 +126,7 @@ KERNEL_SOURCES = {
     "attn_fwd_sm103": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_decode_sm103": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_bwd_sm103": ("bwd_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_fwd_sm103_paged": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
 }
 
 
@@ -391,11 +400,47 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError(f"device error in the timed backward: {eta.attn_status_string(err)}")
         bwd_ms = np.array([e0.elapsed_time(e1) for e0, e1 in b_ev])
 
+    # ---- chunked prefill over a paged cache, in a loop of its own (inputs exceed L2)
+    pp_ms = None
+    ppc = inputs.C6
+    if args.workload in ("both", "prefill") and not args.no_paged_prefill:
+        px = inputs.paged_prefill_config_inputs(ppc, seed=ppc.seed + rank)
+        pq, pkc, pvc = px.q.to(dev), px.k_cache.to(dev), px.v_cache.to(dev)
+        pbt, pql, pkl = px.block_table.to(dev), px.q_lens.to(dev), px.kv_lens.to(dev)
+        po = torch.empty_like(pq)
+        plse = torch.empty(pq.shape[:3], dtype=torch.float32, device=dev)
+        pp_flops = paged_prefill_flops(px.q_lens.tolist(), px.kv_lens.tolist(), ppc.Hq, ppc.d, ppc.causal)
+
+        def run_pp():
+            eta.attn_prefill_paged(pq, pkc, pvc, pbt, pql, pkl, causal=ppc.causal, scale=ppc.scale, out=po, lse=plse)
+
+        for _ in range(args.warmup):
+            run_pp()
+        torch.cuda.synchronize()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the paged prefill warm-up: {eta.attn_status_string(err)}")
+        p_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for e0, e1 in p_ev:
+            e0.record(stream)
+            run_pp()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the timed paged prefill: {eta.attn_status_string(err)}")
+        pp_ms = np.array([e0.elapsed_time(e1) for e0, e1 in p_ev])
+
     # ---- max over ranks
-    vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms +
-                      ([float(bwd_ms.mean())] if bwd_ms is not None else []), world, dev)
-    bwd_mean = vals[-1] if bwd_ms is not None else None
-    vals = vals[:-1] if bwd_ms is not None else vals
+    extra = ([float(bwd_ms.mean())] if bwd_ms is not None else []) + ([float(pp_ms.mean())] if pp_ms is not None else [])
+    vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms + extra, world, dev)
+    pp_mean = vals.pop() if pp_ms is not None else None
+    bwd_mean = vals.pop() if bwd_ms is not None else None
     total_ms, means, e2e_ms = vals[0], vals[1:1 + len(parts)], vals[1 + len(parts):]
     if rank != 0:
         return None
@@ -480,6 +525,24 @@ def run_ours(args, rank, world, local_rank):
                          "traffic": load_traffic("attn_bwd_sm103"),
                          "ms_per_launch": round(bwd_mean, 4),
                          "ms_p10_p50_p90": [round(float(np.percentile(bwd_ms, x)), 4) for x in (10, 50, 90)]},
+        }
+    if pp_ms is not None:
+        achieved = pp_flops / (pp_mean * 1e-3) / 1e12
+        result["paged_prefill"] = {
+            "value": round(whole_job_rate(pp_flops, world, pp_mean, 1e12), 2), "unit": "TFLOP/s",
+            "workload": ppc.name, "flops_per_launch": pp_flops, "steps": args.steps, "warmup": args.warmup,
+            "gpu_launches": args.steps,
+            "config": {"num_seqs": ppc.num_seqs, "Hq": ppc.Hq, "Hkv": ppc.Hkv, "d": ppc.d,
+                       "block_size": ppc.block_size, "q_len": ppc.q_len, "kv_lens": px.kv_lens.tolist(),
+                       "causal": ppc.causal},
+            "roofline": {"kernel": "attn_fwd_sm103<128, paged>", "bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "peak_kind": f"{peak_kind} bf16 dense burst",
+                         "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                         "traffic": load_traffic("attn_fwd_sm103_paged"),
+                         "ms_per_launch": round(pp_mean, 4),
+                         "ms_p10_p50_p90": [round(float(np.percentile(pp_ms, x)), 4) for x in (10, 50, 90)]},
         }
     return result
 
@@ -572,6 +635,7 @@ def main():
     ap.add_argument("--workload", choices=["both", "prefill", "decode"], default="both",
                     help="profiling aid: run only one half of the step (the JSON line then omits the other)")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
+    ap.add_argument("--no-paged-prefill", action="store_true", help="skip the chunked paged prefill measurement")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences than the workload's 64")
     args = ap.parse_args()

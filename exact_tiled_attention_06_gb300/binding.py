@@ -24,7 +24,7 @@ STATUS_NAMES = {
 }
 
 # Every symbol include/attn.h declares.
-EXPORTED = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
+EXPORTED = ("attn_fwd", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
             "attn_decode_noalloc")
 
@@ -56,6 +56,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         lib.attn_fwd.restype = i
+        lib.attn_prefill_paged.argtypes = [vp] * 8 + [i] * 8 + [f, i, i, vp]
+        lib.attn_prefill_paged.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.attn_bwd_workspace_size.restype = sz
         lib.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -135,6 +137,37 @@ def attn_fwd(q, k, v, causal=False, window=-1, scale=None, out=None, lse=None, s
                                  float(scale), int(bool(causal)), int(window), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_prefill_paged(q, k_cache, v_cache, block_table, q_lens, kv_lens, causal=True, window=-1, scale=None,
+                       out=None, lse=None, stream=None):
+    """Paged (chunked) prefill. q [S][Hq][max_q][d] bf16; caches [num_blocks][Hkv][bs][d] bf16;
+    block_table int32 [S][max_blocks]; q_lens, kv_lens int32 [S] (device). Returns (o, lse);
+    rows past q_lens[s] are left as they were in ``out`` / ``lse`` (uninitialised if allocated here)."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(q_lens, "q_lens", torch.int32, 1)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    S, Hq, max_q, d = q.shape
+    nb, Hkv, bs, dk = k_cache.shape
+    if dk != d or v_cache.shape != k_cache.shape or block_table.shape[0] != S or q_lens.shape[0] != S \
+            or kv_lens.shape[0] != S:
+        raise ValueError("paged prefill shapes disagree")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((S, Hq, max_q), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().attn_prefill_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(q_lens),
+                                           _ptr(kv_lens), _ptr(out), _ptr(lse), S, Hq, Hkv, d, bs,
+                                           block_table.shape[1], nb, max_q, float(scale), int(bool(causal)),
+                                           int(window), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_prefill_paged")
     return out, lse
 
 

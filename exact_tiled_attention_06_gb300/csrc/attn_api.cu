@@ -145,6 +145,36 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       static_cast<cudaStream_t>(stream), err);
 }
 
+ATTN_API int attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                const int32_t* q_lens, const int32_t* kv_lens, void* o, float* lse, int num_seqs,
+                                int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq, int num_blocks,
+                                int max_q, float scale, int causal, int window, void* stream)
+{
+    // ---- arguments (no CUDA call before these checks)
+    if (!q || !k_cache || !v_cache || !block_table || !q_lens || !kv_lens || !o || !lse) return kErrInvalidArg;
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || num_blocks <= 0 || max_q < 0)
+        return kErrInvalidArg;
+    if (Hq % Hkv != 0) return kErrInvalidArg;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return kErrInvalidArg;
+    if (static_cast<long long>(num_seqs) * Hq > INT32_MAX / 2) return kErrInvalidArg;
+    if (d != 64 && d != 128) return kErrUnsupported;
+    if (block_size < 16 || block_size > 256 || (block_size & (block_size - 1)) != 0) return kErrUnsupported;
+    if (static_cast<long long>(num_blocks) * Hkv * block_size > INT32_MAX) return kErrUnsupported;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned4(lse) ||
+        !aligned4(block_table) || !aligned4(q_lens) || !aligned4(kv_lens))
+        return kErrMisaligned;
+    if (num_seqs == 0 || max_q == 0) return kOk;
+    // ---- device
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc != kOk) return rc;
+    unsigned* err = device_error_word();
+    if (!err) return kErrCuda;
+    return launch_fwd_paged(q, k_cache, v_cache, block_table, q_lens, kv_lens, o, lse, num_seqs, Hq, Hkv, d,
+                            block_size, max_blocks_per_seq, num_blocks, max_q, scale, causal, window,
+                            static_cast<cudaStream_t>(stream), err);
+}
+
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int d)
 {
     if (B <= 0 || Hq <= 0 || Nq < 0 || (d != 64 && d != 128)) return 0;

@@ -22,6 +22,14 @@
 //
 // Key tiles wholly outside the causal/window band are never visited; the tiles that
 // cross the band edge or the end of the keys are masked per element.
+//
+// PAGED = true is prefill of several sequences against a paged KV cache (chunked
+// prefill): sequence b has q_lens[b] new queries, the last of its kv_lens[b] cached
+// tokens (bottom-right causal alignment), and its keys are read through the block table
+// ("Modern attention kernels", "Paged attention changes addressing"). The producer
+// copies each 128-key tile as min(block_size, 128)-row boxes from the cache's physical
+// blocks and skips blocks past the sequence; in the last, partial tile it zeroes the V
+// rows past the sequence (whatever the cache holds there) before P V may read them.
 #include <climits>
 #include <cmath>
 #include <cuda_bf16.h>
@@ -50,7 +58,7 @@ struct FwdCfg {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + 7;
+    static constexpr int kNumBars = 1 + 2 * kStages + 8;
     static constexpr int kHolderOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kHolderOff + 4;
     static constexpr int kUsedBytes = kAbortOff + 4;
@@ -64,7 +72,11 @@ struct FwdCfg {
 struct FwdParams {
     __nv_bfloat16* o;
     float* lse;
-    int B, Hq, Hkv, Nq, Nk, G;
+    int B, Hq, Hkv, Nq, Nk, G;  // paged: B = sequences, Nq = max_q (row stride), Nk unused
+    const int32_t* block_table;  // paged: [B][max_blocks] physical block of each logical block
+    const int32_t* q_lens;       // paged: [B] new queries per sequence (device)
+    const int32_t* kv_lens;      // paged: [B] cached tokens per sequence, new ones included (device)
+    int max_blocks, block_size, bs_log2, num_blocks;
     float scale_log2;  // scale * log2(e)
     int causal, window;
     int pair_heads;    // 1: tiles are query heads (2u, 2u+1) at one row tile; 0: row tiles (2r, 2r+1)
@@ -83,15 +95,15 @@ struct TileWork {
 
 // Key tiles a query tile must visit: causal keeps keys j <= i + (Nk - Nq); a window
 // w >= 0 also needs j >= i + (Nk - Nq) - w.
-__device__ __forceinline__ TileWork make_tile(const FwdParams& p, int head, int row0)
+__device__ __forceinline__ TileWork make_tile(const FwdParams& p, int head, int row0, int nq, int nk)
 {
     TileWork t{head, row0, 0, 0, 0};
-    int rows = p.Nq - row0;
+    int rows = nq - row0;
     if (rows > BM) rows = BM;
     if (rows <= 0) return t;
     t.rows = rows;
-    const long long delta = static_cast<long long>(p.Nk) - p.Nq;
-    long long key_hi = p.Nk;
+    const long long delta = static_cast<long long>(nk) - nq;
+    long long key_hi = nk;
     if (p.causal) {
         const long long h = static_cast<long long>(row0) + rows + delta;
         if (h < key_hi) key_hi = h;
@@ -109,11 +121,11 @@ __device__ __forceinline__ TileWork make_tile(const FwdParams& p, int head, int 
 }
 
 // True when every key of tile j is allowed for every valid row of the query tile.
-__device__ __forceinline__ bool tile_unmasked(const FwdParams& p, const TileWork& t, int j)
+__device__ __forceinline__ bool tile_unmasked(const FwdParams& p, const TileWork& t, int j, int nq, int nk)
 {
     const long long k0 = static_cast<long long>(j) * BN, k1 = k0 + BN;
-    const long long delta = static_cast<long long>(p.Nk) - p.Nq;
-    if (k1 > p.Nk) return false;
+    const long long delta = static_cast<long long>(nk) - nq;
+    if (k1 > nk) return false;
     if (p.causal && k1 - 1 > t.row0 + delta) return false;
     if (p.window >= 0 && k0 < static_cast<long long>(t.row0) + t.rows - 1 + delta - p.window) return false;
     return true;
@@ -124,7 +136,7 @@ __device__ __forceinline__ bool tile_active(const TileWork& t, int j)
     return t.rows > 0 && t.kv_lo <= j && j < t.kv_hi;
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
@@ -137,20 +149,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work unit (heaviest row units first, which balances the causal triangle)
-    const int n_bh = p.B * p.n_hunits;
+    // ---- work unit. Dense: heaviest row units first, which balances the causal triangle.
+    // Paged: sequence outer, then kv head, then row units (heaviest first) and the head
+    // units of that kv head, so that the blocks running together read the same K/V pages
+    // and the cache stays in L2 (sequences have different lengths; their order is kept).
     const int unit = blockIdx.x;
-    const int ru = p.n_row_units - 1 - unit / n_bh;
-    const int bh = unit % n_bh;
-    const int b = bh / p.n_hunits;
-    const int hu = bh % p.n_hunits;
+    int ru, b, hu;
+    if constexpr (PAGED) {
+        const int per_seq = p.n_hunits * p.n_row_units;
+        const int hpg = p.n_hunits / p.Hkv;  // head units per kv head
+        b = unit / per_seq;
+        const int r = unit % per_seq;
+        const int grp = r / (hpg * p.n_row_units);
+        const int r2 = r % (hpg * p.n_row_units);
+        ru = p.n_row_units - 1 - r2 / hpg;
+        hu = grp * hpg + r2 % hpg;
+    } else {
+        const int n_bh = p.B * p.n_hunits;
+        ru = p.n_row_units - 1 - unit / n_bh;
+        const int bh = unit % n_bh;
+        b = bh / p.n_hunits;
+        hu = bh % p.n_hunits;
+    }
+    // rows and keys of this (batch entry | sequence)
+    int nq = p.Nq, nk = p.Nk;
+    if constexpr (PAGED) {
+        nq = p.q_lens[b];
+        nk = p.kv_lens[b];
+        if (nq < 0 || nq > p.Nq || nk < nq || static_cast<long long>(nk) > static_cast<long long>(p.max_blocks) * p.block_size) {
+            if (threadIdx.x == 0) report_error(p.err, kDevErrBounds);
+            nq = 0;
+            nk = 0;
+        }
+    }
     TileWork tw[2];
     if (p.pair_heads) {
-        tw[0] = make_tile(p, 2 * hu, ru * BM);
-        tw[1] = make_tile(p, 2 * hu + 1, ru * BM);
+        tw[0] = make_tile(p, 2 * hu, ru * BM, nq, nk);
+        tw[1] = make_tile(p, 2 * hu + 1, ru * BM, nq, nk);
     } else {
-        tw[0] = make_tile(p, hu, 2 * ru * BM);
-        tw[1] = make_tile(p, hu, (2 * ru + 1) * BM);
+        tw[0] = make_tile(p, hu, 2 * ru * BM, nq, nk);
+        tw[1] = make_tile(p, hu, (2 * ru + 1) * BM, nq, nk);
     }
     const int hkv = tw[0].head / p.G;
     const bool act[2] = {tw[0].rows > 0 && tw[0].kv_lo < tw[0].kv_hi, tw[1].rows > 0 && tw[1].kv_lo < tw[1].kv_hi};
@@ -173,6 +211,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     auto p_full = [&](int t) { return bar0 + 8u * (3 + 2 * C::kStages + t); };
     auto o_done = [&](int t) { return bar0 + 8u * (5 + 2 * C::kStages + t); };
     const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::kStages);
+    const uint32_t bar_vtail = bar0 + 8u * (8 + 2 * C::kStages);  // paged: the partial tile's V rows zeroed
+    // paged: the key tile that holds the sequence's last key when it is partial, else -1
+    const int tail_j = (PAGED && nk % BN != 0) ? nk / BN : -1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
 
@@ -188,6 +229,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(o_done(t), 1);
         }
         mbar_init(bar_drain, 1);
+        mbar_init(bar_vtail, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -210,7 +252,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     if (warp == kLoadWarp) {
         // ================================================================ producer
-        if (lane == 0 && has_work) {
+        if (has_work && lane == 0) {
             uint32_t qbytes = 0;
 #pragma unroll
             for (int t = 0; t < 2; ++t)
@@ -224,26 +266,107 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     tma_load_3d(sQ + t * C::kTileBytes + x * C::kBoxBytes, &tm_q, bar_q, 64 * x, tw[t].row0,
                                 b * p.Hq + tw[t].head);
             }
-            int n = 0;
+        }
+        int n = 0;  // K/V copies issued (K and V alternate in the ring)
+        if constexpr (!PAGED) {
+            if (has_work && lane == 0) {
+                bool ok = true;
+                for (int j = lo; j < hi && ok; ++j) {
+#pragma unroll
+                    for (int kind = 0; kind < 2; ++kind) {
+                        const int s = n % C::kStages;
+                        if (n >= C::kStages &&
+                            !mbar_wait(kv_empty(s), ((n / C::kStages) - 1) & 1, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(kv_full(s), C::kTileBytes);
+                        const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+#pragma unroll
+                        for (int x = 0; x < C::kBoxes; ++x)
+                            tma_load_3d(sRing + s * C::kTileBytes + x * C::kBoxBytes, map, kv_full(s), 64 * x, j * BN,
+                                        b * p.Hkv + hkv);
+                        ++n;
+                    }
+                }
+            }
+        } else if (has_work) {
+            // Paged: the whole warp. A 128-key tile is `subs` sub-blocks of min(block_size,
+            // 128) rows; lane (u, x) = (lane / kBoxes, lane % kBoxes) copies sub-block u's
+            // column box x, reading its block-table entry one tile ahead. Sub-blocks past the
+            // sequence are not copied.
+            const int sub_rows = p.block_size < BN ? p.block_size : BN;
+            const int subs = BN / sub_rows;
+            const int my_u = lane / C::kBoxes, my_x = lane % C::kBoxes;
+            const bool mine = my_u < subs;
+            auto entry = [&](int jt) -> int {
+                const int key = jt * BN + my_u * sub_rows;
+                return (mine && key < nk) ? __ldg(p.block_table + static_cast<long long>(b) * p.max_blocks +
+                                                  (key >> p.bs_log2))
+                                          : 0;
+            };
+            int ent_next = entry(lo);
             bool ok = true;
             for (int j = lo; j < hi && ok; ++j) {
+                const int ent = ent_next;
+                if (j + 1 < hi) ent_next = entry(j + 1);
+                const int key = j * BN + my_u * sub_rows;
+                const bool copy = mine && key < nk;
+                int row = 0;
+                if (copy) {
+                    int phys = ent;
+                    if (phys < 0 || phys >= p.num_blocks) {
+                        report_error(p.err, kDevErrBounds);
+                        phys = 0;
+                    }
+                    row = (phys * p.Hkv + hkv) * p.block_size + (key & (p.block_size - 1));
+                }
+                const int valid = min(BN, nk - j * BN);  // keys of this tile inside the sequence
+                const int n_sub = (valid + sub_rows - 1) / sub_rows;
 #pragma unroll
                 for (int kind = 0; kind < 2; ++kind) {
                     const int s = n % C::kStages;
-                    if (n >= C::kStages &&
-                        !mbar_wait(kv_empty(s), ((n / C::kStages) - 1) & 1, abort_flag, p.err)) {
+                    bool w = true;
+                    if (lane == 0) {
+                        if (n >= C::kStages) w = mbar_wait(kv_empty(s), ((n / C::kStages) - 1) & 1, abort_flag, p.err);
+                        if (w)
+                            mbar_arrive_expect_tx(kv_full(s), static_cast<uint32_t>(n_sub * sub_rows * 128 * C::kBoxes));
+                    }
+                    if (!__shfl_sync(0xffffffffu, w, 0)) {  // (also orders the copies after expect_tx)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(kv_full(s), C::kTileBytes);
-                    const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
-#pragma unroll
-                    for (int x = 0; x < C::kBoxes; ++x)
-                        tma_load_3d(sRing + s * C::kTileBytes + x * C::kBoxBytes, map, kv_full(s), 64 * x, j * BN,
-                                    b * p.Hkv + hkv);
+                    const uint32_t dst = sRing + s * C::kTileBytes;
+                    if (copy)
+                        tma_load_2d(dst + my_x * C::kBoxBytes + my_u * sub_rows * 128, kind == 0 ? &tm_k : &tm_v,
+                                    kv_full(s), 64 * my_x, row);
                     ++n;
+                    if (kind == 1 && j == tail_j) {
+                        // V of the partial tile: once it has landed, zero the rows past the
+                        // sequence (stale or unwritten cache slots) so that P V never meets a
+                        // NaN under a zero weight; then hand the tile to the MMA thread
+                        bool f = true;
+                        if (lane == 0) f = mbar_wait(kv_full(s), ((n - 1) / C::kStages) & 1, abort_flag, p.err);
+                        if (!__shfl_sync(0xffffffffu, f, 0)) {
+                            ok = false;
+                            break;
+                        }
+                        for (int r = valid + lane; r < BN; r += 32)
+#pragma unroll
+                            for (int x = 0; x < C::kBoxes; ++x)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                                                 ::"r"(dst + x * C::kBoxBytes + r * 128 + 16 * c), "r"(0u)
+                                                 : "memory");
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_vtail);
+                    }
                 }
             }
+        }
+        if (has_work && lane == 0) {
             // Never leave while a copy into this block's shared memory is in flight.
             mbar_wait(bar_q, 0, nullptr, p.err);
             for (int s = 0; s < C::kStages; ++s) {
@@ -309,6 +432,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int j = lo; j < hi && ok; ++j) {
                 const int vs = n % C::kStages;
                 if (!mbar_wait(kv_full(vs), (n / C::kStages) & 1, abort_flag, p.err)) break;
+                // paged: the partial tile's V is usable once its tail rows are zeroed
+                if (PAGED && j == tail_j && !mbar_wait(bar_vtail, 0, abort_flag, p.err)) break;
                 tc_fence_after();
                 ++n;
                 const bool has_next = j + 1 < hi;
@@ -370,8 +495,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         bool ok = true;
         const bool tile_has = t ? act[1] : act[0];
         if (tile_has) {
-            const long long diag = static_cast<long long>(row) + (static_cast<long long>(p.Nk) - p.Nq);
-            long long key_max = static_cast<long long>(p.Nk) - 1;
+            const long long diag = static_cast<long long>(row) + (static_cast<long long>(nk) - nq);
+            long long key_max = static_cast<long long>(nk) - 1;
             if (p.causal && diag < key_max) key_max = diag;
             const long long key_min = p.window >= 0 ? diag - p.window : LLONG_MIN / 4;
             for (int j = T.kv_lo; j < T.kv_hi; ++j) {
@@ -388,7 +513,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 float s[BN];
 #pragma unroll
                 for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
-                if (!tile_unmasked(p, T, j)) {
+                if (!tile_unmasked(p, T, j, nq, nk)) {
                     const long long kbase = static_cast<long long>(j) * BN;
                     long long hi_rel = key_max - kbase;
                     long long lo_rel = key_min - kbase;
@@ -459,7 +584,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // ---- epilogue: O / l -> bf16, lse = ln2 * (m + log2 l)
         if (T.rows > 0 && ok) {
-            const bool valid_row = row < p.Nq;
+            const bool valid_row = row < nq;
             const size_t row_idx = (static_cast<size_t>(b) * p.Hq + T.head) * p.Nq + row;
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
             if (tile_has) {
@@ -550,15 +675,80 @@ int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* ls
     const int n_row_tiles = (Nq + BM - 1) / BM;
     prm.n_row_units = prm.pair_heads ? n_row_tiles : (n_row_tiles + 1) / 2;
     prm.n_hunits = prm.pair_heads ? Hq / 2 : Hq;
+    prm.block_table = nullptr;
+    prm.q_lens = nullptr;
+    prm.kv_lens = nullptr;
+    prm.max_blocks = prm.block_size = prm.bs_log2 = prm.num_blocks = 0;
     prm.err = err;
     const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
     if (grid > INT_MAX) return kErrInvalidArg;
 
-    if (cudaFuncSetAttribute(attn_fwd_sm103<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+    if (cudaFuncSetAttribute(attn_fwd_sm103<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return kErrCuda;
-    attn_fwd_sm103<D><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    attn_fwd_sm103<D, false><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+}
+
+// Paged prefill: q, o [S][Hq][max_q][d]; caches [num_blocks][Hkv][block_size][d] read
+// through 2-D TMA views {d, num_blocks * Hkv * block_size} with min(block_size, 128)-row
+// boxes. Arguments are already validated (block_size a power of two in [16, 256]).
+template <int D>
+int launch_fwd_paged_d(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* q_lens, const int32_t* kv_lens, void* o, float* lse, int S, int Hq, int Hkv,
+                       int block_size, int max_blocks, int num_blocks, int max_q, float scale, int causal, int window,
+                       cudaStream_t stream, unsigned* err)
+{
+    using C = FwdCfg<D>;
+    CUtensorMap tq, tk, tv;
+    {
+        const uint32_t box[3] = {64u, 128u, 1u};
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(max_q), static_cast<uint64_t>(S) * Hq};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(max_q) * D * 2};
+        int rc = encode_bf16_map(&tq, q, 3, dims, strides, box);
+        if (rc != kOk) return rc;
+    }
+    {
+        const uint32_t box[2] = {64u, static_cast<uint32_t>(block_size < BN ? block_size : BN)};
+        const uint64_t dims[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(num_blocks) * Hkv * block_size};
+        const uint64_t strides[1] = {static_cast<uint64_t>(D) * 2};
+        int rc = encode_bf16_map(&tk, k_cache, 2, dims, strides, box);
+        if (rc != kOk) return rc;
+        rc = encode_bf16_map(&tv, v_cache, 2, dims, strides, box);
+        if (rc != kOk) return rc;
+    }
+    FwdParams prm;
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = S;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Nq = max_q;
+    prm.Nk = 0;
+    prm.G = Hq / Hkv;
+    prm.block_table = block_table;
+    prm.q_lens = q_lens;
+    prm.kv_lens = kv_lens;
+    prm.max_blocks = max_blocks;
+    prm.block_size = block_size;
+    prm.bs_log2 = 31 - __builtin_clz(static_cast<unsigned>(block_size));
+    prm.num_blocks = num_blocks;
+    prm.scale_log2 = scale * kLog2e;
+    prm.causal = causal ? 1 : 0;
+    prm.window = window < 0 ? -1 : window;
+    prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+    const int n_row_tiles = (max_q + BM - 1) / BM;
+    prm.n_row_units = prm.pair_heads ? n_row_tiles : (n_row_tiles + 1) / 2;
+    prm.n_hunits = prm.pair_heads ? Hq / 2 : Hq;
+    prm.err = err;
+    const long long grid = static_cast<long long>(S) * prm.n_hunits * prm.n_row_units;
+    if (grid <= 0) return kOk;
+    if (grid > INT_MAX) return kErrInvalidArg;
+    if (cudaFuncSetAttribute(attn_fwd_sm103<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return kErrCuda;
+    attn_fwd_sm103<D, true><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 
@@ -570,6 +760,21 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     if (Nq == 0) return kOk;
     if (d == 128) return launch_fwd_d<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream, err);
     if (d == 64) return launch_fwd_d<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream, err);
+    return kErrUnsupported;
+}
+
+int launch_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                     const int32_t* q_lens, const int32_t* kv_lens, void* o, float* lse, int S, int Hq, int Hkv, int d,
+                     int block_size, int max_blocks, int num_blocks, int max_q, float scale, int causal, int window,
+                     cudaStream_t stream, unsigned* err)
+{
+    if (S == 0 || max_q == 0) return kOk;
+    if (d == 128)
+        return launch_fwd_paged_d<128>(q, k_cache, v_cache, block_table, q_lens, kv_lens, o, lse, S, Hq, Hkv,
+                                       block_size, max_blocks, num_blocks, max_q, scale, causal, window, stream, err);
+    if (d == 64)
+        return launch_fwd_paged_d<64>(q, k_cache, v_cache, block_table, q_lens, kv_lens, o, lse, S, Hq, Hkv,
+                                      block_size, max_blocks, num_blocks, max_q, scale, causal, window, stream, err);
     return kErrUnsupported;
 }
 

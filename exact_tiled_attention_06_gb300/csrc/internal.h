@@ -41,6 +41,12 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nq, int Nk, int d, float scale, int causal, int window, cudaStream_t stream,
                unsigned* err);
 
+// Paged prefill (implemented in fwd_kernel.cu). Arguments are already validated.
+int launch_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                     const int32_t* q_lens, const int32_t* kv_lens, void* o, float* lse, int S, int Hq, int Hkv, int d,
+                     int block_size, int max_blocks, int num_blocks, int max_q, float scale, int causal, int window,
+                     cudaStream_t stream, unsigned* err);
+
 // Split-KV decode plan: the chunk length and the workspace carve-up.
 struct DecodePlan {
     int chunk;              // keys per split (multiple of 16 and of block_size)

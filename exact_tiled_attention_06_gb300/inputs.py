@@ -16,6 +16,9 @@ Recipe (one ``torch.Generator`` on the CPU per call, seeded explicitly):
   iid N(0, 1) rounded to bf16. The block table lists each sequence's physical
   blocks in logical order; unused entries are -1. ``poison`` fills every cache
   slot that no sequence owns (tail slots of a last block, unused blocks) with NaN.
+* paged prefill: the cache and table of the decode recipe for the sequences'
+  kv lengths (query lengths drawn first when not given), then q [S][Hq][max_q][d]
+  from a generator seeded apart; ``poison`` also fills q rows past each q_len with NaN.
 """
 from __future__ import annotations
 
@@ -65,6 +68,25 @@ class DecodeConfig:
         return 1.0 / math.sqrt(self.d)
 
 
+@dataclass(frozen=True)
+class PagedPrefillConfig:
+    name: str
+    num_seqs: int
+    Hq: int
+    Hkv: int
+    d: int
+    block_size: int
+    q_len: int              # new queries per sequence (a prefill chunk)
+    ctx_lo: int             # cached tokens before the chunk, uniform integers in [ctx_lo, ctx_hi]
+    ctx_hi: int
+    causal: bool = True
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
 # The five workloads (shapes of the pages' examples: N=512/d=64 single head;
 # 2k and 8k causal prefill with d=128; GQA with 4 query heads per kv head and a
 # sliding window; paged GQA decode with 16-token pages and up to 32k context).
@@ -76,7 +98,13 @@ C4 = PrefillConfig("C4_gqa_causal_window1024_B2_Hq32_Hkv8_N4096_d128", 2, 32, 8,
                    window=1024)
 C5 = DecodeConfig("C5_paged_gqa_decode_S64_Hq32_Hkv8_d128_bs16_L1k_32k", 64, 32, 8, 128, 16, 1024, 32768)
 
+# Chunked prefill over a paged cache (the pages give no numbers for it): 16 sequences,
+# each appending a 2048-token chunk to 0..14336 earlier tokens, GQA 32/8, 16-token blocks.
+C6 = PagedPrefillConfig("C6_chunked_prefill_paged_S16_q2048_ctx0_14k_Hq32_Hkv8_d128_bs16", 16, 32, 8, 128, 16,
+                        2048, 0, 14336)
+
 PREFILL_CONFIGS = {c.name: c for c in (C1, C2, C3, C4)}
+PAGED_PREFILL_CONFIGS = {C6.name: C6}
 DECODE_CONFIGS = {C5.name: C5}
 
 
@@ -184,3 +212,42 @@ def decode_config_inputs(cfg: DecodeConfig, seed=None, poison=False):
     return decode_inputs(cfg.num_seqs, cfg.Hq, cfg.Hkv, cfg.d, cfg.block_size, len_lo=cfg.len_lo,
                          len_hi=cfg.len_hi, seed=cfg.seed if seed is None else seed,
                          extra_blocks=cfg.extra_blocks, poison=poison)
+
+
+@dataclass
+class PagedPrefillInputs:
+    q: torch.Tensor            # [S][Hq][max_q][d] bf16
+    k_cache: torch.Tensor      # [num_blocks][Hkv][bs][d] bf16
+    v_cache: torch.Tensor
+    block_table: torch.Tensor  # [S][max_blocks] int32, -1 = unused
+    q_lens: torch.Tensor       # [S] int32
+    kv_lens: torch.Tensor      # [S] int32
+    block_size: int
+
+
+def paged_prefill_inputs(num_seqs, Hq, Hkv, d, block_size, q_lens, kv_lens, max_q=None, seed=0, extra_blocks=0,
+                         poison=False, identity_table=False, max_blocks_per_seq=None):
+    """Paged prefill inputs for given per-sequence query and cache lengths."""
+    assert len(q_lens) == num_seqs and len(kv_lens) == num_seqs
+    assert all(0 <= a <= b for a, b in zip(q_lens, kv_lens))
+    x = decode_inputs(num_seqs, Hq, Hkv, d, block_size, seq_lens=list(kv_lens), seed=seed, extra_blocks=extra_blocks,
+                      poison=poison, identity_table=identity_table, max_blocks_per_seq=max_blocks_per_seq)
+    max_q = max(q_lens) if max_q is None else max_q
+    gen = torch.Generator().manual_seed(int(seed) * 7919 + 31337)
+    q = _bf16_normal(gen, (num_seqs, Hq, max_q, d))
+    if poison:
+        for s, n in enumerate(q_lens):
+            q[s, :, n:, :] = float("nan")
+    return PagedPrefillInputs(q=q, k_cache=x.k_cache, v_cache=x.v_cache, block_table=x.block_table,
+                              q_lens=torch.as_tensor(list(q_lens), dtype=torch.int32),
+                              kv_lens=torch.as_tensor(list(kv_lens), dtype=torch.int32), block_size=block_size)
+
+
+def paged_prefill_config_inputs(cfg: PagedPrefillConfig, seed=None):
+    """The chunked-prefill workload: context lengths drawn first, then the cache and q."""
+    sd = cfg.seed if seed is None else seed
+    gen = torch.Generator().manual_seed(int(sd) * 104729 + 7)
+    ctx = torch.randint(cfg.ctx_lo, cfg.ctx_hi + 1, (cfg.num_seqs,), generator=gen, dtype=torch.int64)
+    q_lens = [cfg.q_len] * cfg.num_seqs
+    kv_lens = [int(c) + cfg.q_len for c in ctx]
+    return paged_prefill_inputs(cfg.num_seqs, cfg.Hq, cfg.Hkv, cfg.d, cfg.block_size, q_lens, kv_lens, seed=sd)

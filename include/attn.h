@@ -73,6 +73,40 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int causal, int window, void* stream);
 
 /*
+ * attn_prefill_paged -- prefill of several sequences against a paged KV cache (chunked
+ * prefill): each sequence's new queries attend to its cached tokens, the new ones included.
+ *
+ *   MAK "Paged attention changes addressing" (logical block = pos / block_size, offset =
+ *   pos % block_size, physical = block_table[seq, block], address = base + physical *
+ *   block_stride + offset * token_stride); MAK "Prefill and decode need different
+ *   kernels" and AK (tiled prefill, paged cache: one engine uses both), with the tiled
+ *   online-softmax computation of attn_fwd.
+ *
+ *   q          : bf16 [num_seqs][Hq][max_q][d]      (input) rows i >= q_lens[s] are not read
+ *   k_cache,
+ *   v_cache    : bf16 [num_blocks][Hkv][block_size][d] (input, layout version 1)
+ *   block_table: int32 [num_seqs][max_blocks_per_seq] (input, device)
+ *   q_lens     : int32 [num_seqs] (device) new queries of each sequence, 0 <= q_len <= max_q
+ *   kv_lens    : int32 [num_seqs] (device) tokens of each sequence in the cache, new ones
+ *                included: q_len <= kv_len <= max_blocks_per_seq * block_size. Query row i
+ *                of sequence s is position kv_len - q_len + i (bottom-right alignment).
+ *   o          : bf16 [num_seqs][Hq][max_q][d]      (output) rows i >= q_lens[s] untouched
+ *   lse        : fp32 [num_seqs][Hq][max_q]         (output) as attn_fwd; rows past q_len untouched
+ *   block_size : a power of two in [16, 256]. causal, window, scale: as attn_fwd, with
+ *                Nq = q_len and Nk = kv_len per sequence.
+ *   Cache slots past a sequence's end (the tail of its last block) are never used, whatever
+ *   they hold. A block-table entry outside [0, num_blocks), or lengths breaking the bounds
+ *   above, set ATTN_ERR_DEVICE_BOUNDS in the device error word (that sequence's output is
+ *   then undefined). num_blocks * Hkv * block_size must stay below 2^31.
+ *   Enqueues one kernel on `stream`. Returns ATTN_OK or a negative attn_status.
+ */
+int attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* q_lens, const int32_t* kv_lens,
+                       void* o, float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
+                       int max_blocks_per_seq, int num_blocks, int max_q, float scale,
+                       int causal, int window, void* stream);
+
+/*
  * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: D_i = rowsum(dO o O) in
  * fp32 [B][Hq][Nq] (256-byte aligned), then an fp32 dQ accumulator [B][Hq][Nq][d].
  * Returns 0 for invalid sizes.

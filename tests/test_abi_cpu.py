@@ -104,6 +104,30 @@ def test_bwd_workspace_size(lib):
     assert eta.attn_bwd_workspace_size(0, 4, 200, 64) == 0
 
 
+def ppf(lib, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, ql=FAKE, kl=FAKE, o=FAKE, lse=FAKE, S=4, Hq=8, Hkv=2, d=128, bs=16,
+        mb=64, nb=256, max_q=300, scale=0.1, causal=1, window=-1):
+    return lib.attn_prefill_paged(q, kc, vc, bt, ql, kl, o, lse, S, Hq, Hkv, d, bs, mb, nb, max_q, scale, causal,
+                                  window, None)
+
+
+def test_prefill_paged_argument_validation(lib):
+    assert ppf(lib, q=None) == -1
+    assert ppf(lib, kl=None) == -1
+    assert ppf(lib, Hq=6, Hkv=4) == -1
+    assert ppf(lib, nb=0) == -1
+    assert ppf(lib, max_q=-1) == -1
+    assert ppf(lib, scale=0.0) == -1
+    assert ppf(lib, d=32) == -2
+    assert ppf(lib, bs=8) == -2              # below 16
+    assert ppf(lib, bs=48) == -2             # not a power of two
+    assert ppf(lib, bs=512) == -2            # above 256
+    assert ppf(lib, nb=1 << 26) == -2        # cache rows past 2^31
+    assert ppf(lib, o=FAKE + 8) == -3
+    assert ppf(lib, ql=FAKE + 2) == -3
+    assert ppf(lib, S=0) == 0                # nothing to do: no launch
+    assert ppf(lib, max_q=0) == 0
+
+
 def dec(lib, ws_bytes=None, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, o=FAKE, lse=FAKE, S=4, Hq=8, Hkv=2, d=128,
         bs=16, mb=64, nb=256, scale=0.1, ws=FAKE):
     if ws_bytes is None:

@@ -52,3 +52,13 @@ def test_backward_flops_are_five_matmuls():
         assert bench.backward_flops(*args) * 2 == bench.attention_flops(*args) * 5
     # one head, no mask: 10 N^2 d
     assert bench.backward_flops(1, 1, 64, 64, 128) == 10 * 64 * 64 * 128
+
+
+def test_paged_prefill_flops():
+    """Per sequence, the prefill count with Nq = q_len and Nk = kv_len."""
+    q, kv = [2048, 5, 0, 1], [4096, 5, 7, 9000]
+    want = sum(bench.attention_flops(1, 32, a, b, 128, True) for a, b in zip(q, kv))
+    assert bench.paged_prefill_flops(q, kv, 32, 128, True) == want
+    # a whole prompt (q_len = kv_len) equals causal prefill; one query sees every key
+    assert bench.paged_prefill_flops([300], [300], 4, 64, True) == bench.attention_flops(1, 4, 300, 300, 64, True)
+    assert bench.paged_prefill_flops([1], [77], 1, 64, True) == 4 * 64 * 77
