@@ -26,6 +26,9 @@ What each function follows (pages by title and section):
 * ``attn_decode`` -- one query per sequence over a paged cache, addressed with
   the block-table formula of "Modern attention kernels",
   "Paged attention changes addressing".
+* ``attn_fwd_blocksparse`` -- prefill restricted to the score blocks a CSR block index
+  lists ("Modern attention kernels", "Kernel structure" and the table of variants),
+  materialised per row with the block membership added to the mask.
 * ``attn_prefill_paged`` -- several new queries per sequence over a paged cache
   (chunked prefill): the keys are gathered with the same formula and each new row
   goes through the materialised row routine, bottom-right causal.
@@ -80,12 +83,14 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attn_fwd_split.argtypes = [_D, _D, _D, _D, _D] + [c_int] * 6 + [c_double, c_int, c_int, c_int]
     lib.oracle_attn_decode.argtypes = [_D, _D, _D, _I32, _I32, _D, _D] + [c_int] * 7 + [c_double]
     lib.oracle_attn_bwd.argtypes = [_D] * 7 + [c_int] * 6 + [c_double, c_int, c_int]
+    lib.oracle_attn_fwd_blocksparse.argtypes = [_D] * 5 + [c_int] * 6 + [c_double, c_int, c_int, _I32, _I32, c_int,
+                                                                             c_int]
     lib.oracle_attn_prefill_paged.argtypes = [_D, _D, _D, _I32, _I32, _I32, _D, _D] + [c_int] * 8 + [c_double, c_int,
                                                                                                    c_int]
     lib.oracle_num_threads.argtypes = []
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows, lib.oracle_attn_fwd_blocked,
               lib.oracle_attn_fwd_split, lib.oracle_attn_decode, lib.oracle_attn_bwd, lib.oracle_attn_prefill_paged,
-              lib.oracle_num_threads):
+              lib.oracle_attn_fwd_blocksparse, lib.oracle_num_threads):
         f.restype = c_int
     return lib
 
@@ -191,6 +196,25 @@ class Oracle:
                                         Nk, d, float(scale), int(bool(causal)), int(window)), "oracle_attn_bwd")
         return dq, dk, dv
 
+    def attn_fwd_blocksparse(self, q, k, v, row_ptr, col_idx, scale, causal=False, window=-1, block_q=128,
+                             block_k=128):
+        """Block-sparse attention: (row_ptr, col_idx) list the key blocks of each query block."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, Nq, Nk, d = _shapes(q, k, v)
+        rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+        ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+        if rp.shape != ((Nq + block_q - 1) // block_q + 1,):
+            raise ValueError("row_ptr must have one entry per query block plus one")
+        if ci.size == 0:
+            ci = np.zeros(1, dtype=np.int32)
+        o = np.zeros((B, Hq, Nq, d))
+        lse = np.zeros((B, Hq, Nq))
+        _check(self.lib.oracle_attn_fwd_blocksparse(_p(q), _p(k), _p(v), _p(o), _p(lse), B, Hq, Hkv, Nq, Nk, d,
+                                                    float(scale), int(bool(causal)), int(window),
+                                                    rp.ctypes.data_as(_I32), ci.ctypes.data_as(_I32), int(block_q),
+                                                    int(block_k)), "oracle_attn_fwd_blocksparse")
+        return o, lse
+
     def attn_prefill_paged(self, q, k_cache, v_cache, block_table, q_lens, kv_lens, scale, causal=True, window=-1):
         """Paged prefill. q [S][Hq][max_q][d]; caches [num_blocks][Hkv][bs][d]; block_table int32
         [S][max_blocks]; q_lens, kv_lens int32 [S]. Returns (o, lse) shaped like q and [S][Hq][max_q];
@@ -266,6 +290,10 @@ def attn_bwd(*a, **kw):
 
 def attn_prefill_paged(*a, **kw):
     return default().attn_prefill_paged(*a, **kw)
+
+
+def attn_fwd_blocksparse(*a, **kw):
+    return default().attn_fwd_blocksparse(*a, **kw)
 
 
 def num_threads() -> int:

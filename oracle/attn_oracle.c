@@ -419,6 +419,88 @@ int oracle_attn_decode(const double* q, const double* k_cache, const double* v_c
 }
 
 /* ------------------------------------------------------------------------- */
+/* Block-sparse prefill.                                                        */
+/* [MAK] "Kernel structure": an arbitrary sparse mask needs an index telling   */
+/*   the kernel which blocks exist; [MAK] (the table of attention variants):   */
+/*   sparse attention visits only the selected score blocks.                  */
+/* Reading: a CSR index over (query block of block_q rows, key block of         */
+/* block_k keys): row_ptr[n_qblk + 1], col_idx[nnz], shared by every batch     */
+/* entry and head. Query row i may attend key j when the block pair            */
+/* (i / block_q, j / block_k) is listed AND the causal / window mask of the    */
+/* dense functions allows it. Materialised per row, like the plain definition. */
+/* ------------------------------------------------------------------------- */
+static int block_listed(const int32_t* row_ptr, const int32_t* col_idx, long qb, long kb)
+{
+    for (long e = row_ptr[qb]; e < row_ptr[qb + 1]; ++e)
+        if (col_idx[e] == kb) return 1;
+    return 0;
+}
+
+int oracle_attn_fwd_blocksparse(const double* q, const double* k, const double* v, double* o, double* lse,
+                                int B, int Hq, int Hkv, int Nq, int Nk, int d, double scale, int causal, int window,
+                                const int32_t* row_ptr, const int32_t* col_idx, int block_q, int block_k)
+{
+    if (check_dims(B, Hq, Hkv, Nq, Nk, d) || block_q <= 0 || block_k <= 0) return ORACLE_EINVAL;
+    long n_qblk = (Nq + block_q - 1) / block_q, n_kblk = (Nk + block_k - 1) / block_k;
+    if (row_ptr[0] != 0) return ORACLE_EINVAL;
+    for (long qb = 0; qb < n_qblk; ++qb) {
+        if (row_ptr[qb + 1] < row_ptr[qb]) return ORACLE_EINVAL;
+        for (long e = row_ptr[qb]; e < row_ptr[qb + 1]; ++e)
+            if (col_idx[e] < 0 || col_idx[e] >= n_kblk) return ORACLE_EBOUNDS;
+    }
+    int G = Hq / Hkv;
+    int err = ORACLE_OK;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        if (!s || !p) {
+#pragma omp atomic write
+            err = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 16) collapse(2)
+            for (long bh = 0; bh < (long)B * Hq; ++bh) {
+                for (long i = 0; i < Nq; ++i) {
+                    long b = bh / Hq, h = bh % Hq, hk = h / G;
+                    const double* qi = q + ((bh * (long)Nq + i) * d);
+                    const double* kh = k + ((b * Hkv + hk) * (long)Nk * d);
+                    const double* vh = v + ((b * Hkv + hk) * (long)Nk * d);
+                    double* oi = o + ((bh * (long)Nq + i) * d);
+                    /* scores of the allowed keys, -inf elsewhere */
+                    double m = -INFINITY;
+                    for (long j = 0; j < Nk; ++j) {
+                        if (key_allowed(i, j, Nq, Nk, causal, window) &&
+                            block_listed(row_ptr, col_idx, i / block_q, j / block_k))
+                            s[j] = dot(qi, kh + j * d, d) * scale;
+                        else
+                            s[j] = -INFINITY;
+                        if (s[j] > m) m = s[j];
+                    }
+                    for (int t = 0; t < d; ++t) oi[t] = 0.0;
+                    if (m == -INFINITY) {
+                        lse[bh * (long)Nq + i] = -INFINITY;
+                        continue;
+                    }
+                    double l = 0.0;
+                    for (long j = 0; j < Nk; ++j) {
+                        p[j] = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - m);
+                        l += p[j];
+                    }
+                    for (long j = 0; j < Nk; ++j) {
+                        if (p[j] == 0.0) continue;
+                        for (int t = 0; t < d; ++t) oi[t] += (p[j] / l) * vh[j * d + t];
+                    }
+                    lse[bh * (long)Nq + i] = m + log(l);
+                }
+            }
+        }
+        free(s);
+        free(p);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Prefill of several sequences against a paged cache (chunked prefill).       */
 /* [MAK] "Paged attention changes addressing": token t of a sequence sits in   */
 /*   logical block t / block_size at offset t % block_size; the block table    */

@@ -445,6 +445,75 @@ def pin_paged_prefill_equals_gathered_prefill(orc):
                 _close(lse[s, :, :ql[s]], lf[0], 1e-14, f"paged prefill bs={bs} seq{s} lse")
 
 
+def _csr(pattern):
+    """Dense boolean block pattern [n_qblk][n_kblk] -> (row_ptr, col_idx)."""
+    rows = [np.flatnonzero(r).astype(np.int32) for r in np.asarray(pattern, dtype=bool)]
+    row_ptr = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    col_idx = np.concatenate(rows).astype(np.int32) if sum(len(r) for r in rows) else np.zeros(0, np.int32)
+    return row_ptr, col_idx
+
+
+def pin_blocksparse_full_pattern_is_dense(orc):
+    """Every block listed: exactly the dense masks."""
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        q, k, v = _qkv(1900 + mi, 1, 4, 2, Nq, Nk, 4)
+        for bq, bk in ((3, 5), (4, 4), (Nq, Nk)):
+            nqb, nkb = -(-Nq // bq), -(-Nk // bk)
+            rp, ci = _csr(np.ones((nqb, nkb)))
+            o, lse = orc.attn_fwd_blocksparse(q, k, v, rp, ci, 0.5, causal, window, bq, bk)
+            od, ld = orc.attn_fwd(q, k, v, 0.5, causal, window)
+            _close(o, od, 1e-14, f"full pattern O {mi} ({bq},{bk})")
+            _close(lse, ld, 1e-14, f"full pattern lse {mi} ({bq},{bk})")
+
+
+def pin_blocksparse_numpy_bruteforce(orc):
+    """Random block patterns (empty block rows included), unequal block sizes: the element
+    mask is the block pattern expanded with numpy, intersected with the dense mask."""
+    r = _rng(1950)
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS):
+        bq, bk = 2, 3
+        nqb, nkb = -(-Nq // bq), -(-Nk // bk)
+        pat = r.random((nqb, nkb)) < 0.5
+        pat[0, :] = False  # an empty block row
+        rp, ci = _csr(pat)
+        q, k, v = _qkv(1960 + mi, 1, 2, 1, Nq, Nk, 3)
+        o, lse = orc.attn_fwd_blocksparse(q, k, v, rp, ci, 0.7, causal, window, bq, bk)
+        i = np.arange(Nq)[:, None]
+        j = np.arange(Nk)[None, :]
+        diag = i + (Nk - Nq)
+        keep = pat[i // bq, j // bk]
+        if causal:
+            keep = keep & (j <= diag)
+        if window >= 0:
+            keep = keep & (j >= diag - window)
+        s = 0.7 * np.einsum("bhid,bhjd->bhij", q, np.repeat(k, 2, axis=1))
+        s = np.where(keep, s, -np.inf)
+        m = s.max(axis=-1, keepdims=True)
+        e = np.where(keep, np.exp(s - np.where(np.isfinite(m), m, 0.0)), 0.0)
+        l = e.sum(axis=-1, keepdims=True)
+        pr = np.divide(e, l, out=np.zeros_like(e), where=l > 0)
+        ref_o = np.einsum("bhij,bhjd->bhid", pr, np.repeat(v, 2, axis=1))
+        ref_lse = np.where(l[..., 0] > 0, m[..., 0] + np.log(np.where(l[..., 0] > 0, l[..., 0], 1.0)), -np.inf)
+        _close(o, ref_o, 1e-13, f"blocksparse numpy O {mi}")
+        assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lse)), "blocksparse empty-row pattern"
+        fin = np.isfinite(ref_lse)
+        _close(lse[fin], ref_lse[fin], 1e-13, f"blocksparse numpy lse {mi}")
+
+
+def pin_blocksparse_block_diagonal_is_segments(orc):
+    """A block-diagonal pattern (equal block sizes, no other mask) splits the sequence into
+    independent segments: each equals plain attention on its slice."""
+    N, b = 12, 4
+    q, k, v = _qkv(1990, 1, 2, 2, N, N, 5)
+    rp, ci = _csr(np.eye(N // b, dtype=bool))
+    o, lse = orc.attn_fwd_blocksparse(q, k, v, rp, ci, 0.4, False, -1, b, b)
+    for t in range(N // b):
+        sl = slice(t * b, (t + 1) * b)
+        os_, ls_ = orc.attn_fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], 0.4)
+        _close(o[:, :, sl], os_, 1e-14, f"segment {t} O")
+        _close(lse[:, :, sl], ls_, 1e-14, f"segment {t} lse")
+
+
 ALL_PINS = [
     pin_blocked_equals_materialised,
     pin_split_equals_unsplit,
@@ -466,4 +535,7 @@ ALL_PINS = [
     pin_bwd_gqa_equals_duplicated_heads,
     pin_paged_prefill_single_query_is_decode,
     pin_paged_prefill_equals_gathered_prefill,
+    pin_blocksparse_full_pattern_is_dense,
+    pin_blocksparse_numpy_bruteforce,
+    pin_blocksparse_block_diagonal_is_segments,
 ]

@@ -35,6 +35,11 @@ MUTANTS = [
     ("paged_prefill_no_head_offset", "off * token_stride + hk * (long)block_size * d;", "off * token_stride;"),
     ("paged_prefill_top_left_alignment", "kh, vh, i, qn, kn, d, scale", "kh, vh, i, kn, kn, d, scale"),
     ("paged_prefill_offset_by_block", "off = t % block_size;", "off = t / block_size;"),
+    ("blocksparse_pattern_ignored", "&&\n                            block_listed(row_ptr, col_idx, i / block_q, j / block_k))",
+     "&& 1)"),
+    ("blocksparse_dense_mask_ignored", "if (key_allowed(i, j, Nq, Nk, causal, window) &&\n                            block_listed",
+     "if (j < Nk &&\n                            block_listed"),
+    ("blocksparse_key_block_by_query_size", "i / block_q, j / block_k))", "i / block_q, j / block_q))"),
 ]
 
 
