@@ -12,7 +12,9 @@ so no flush is needed between steps. ``backward`` times attn_bwd on the prefill
 workload in a loop of its own after the step (same warm-up and step counts;
 10 * d FLOPs per allowed pair); ``--no-backward`` skips it. ``paged_prefill`` times
 attn_prefill_paged on the chunked-prefill workload (16 sequences, 2048 new queries
-each over a paged cache) the same way; ``--no-paged-prefill`` skips it.
+each over a paged cache) the same way; ``--no-paged-prefill`` skips it. ``blocksparse``
+times attn_fwd_blocksparse on a 32k-token global + local block pattern the same way
+(4 * d FLOPs per allowed pair of the listed blocks); ``--no-blocksparse`` skips it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -74,6 +76,24 @@ def paged_prefill_flops(q_lens, kv_lens, Hq, d, causal=True, window=-1) -> int:
     return int(sum(4 * d * allowed_pairs(int(a), int(b), causal, window) * Hq for a, b in zip(q_lens, kv_lens)))
 
 
+def blocksparse_pairs(pattern, Nq, Nk, causal, window, block=128) -> int:
+    """Allowed (query, key) pairs of one head under a block pattern [n_qblk][n_kblk], counted
+    exactly per listed block pair with the causal / window mask (bottom-right alignment)."""
+    pat = np.asarray(pattern, dtype=bool)
+    delta = Nk - Nq
+    total = 0
+    for r, c in zip(*np.nonzero(pat)):
+        i = np.arange(r * block, min((r + 1) * block, Nq), dtype=np.int64)
+        lo = np.full(i.shape, c * block, dtype=np.int64)
+        hi = np.full(i.shape, min((c + 1) * block, Nk), dtype=np.int64)
+        if causal:
+            hi = np.minimum(hi, i + delta + 1)
+        if window >= 0:
+            lo = np.maximum(lo, i + delta - window)
+        total += int(np.maximum(hi - lo, 0).sum())
+    return total
+
+
 def score_matrix_bytes(N: int, bytes_per_el: int = 2) -> int:
     """Size of one head's N x N score matrix."""
     return N * N * bytes_per_el
@@ -127,6 +147,7 @@ KERNEL_SOURCES = {
     "attn_decode_sm103": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_bwd_sm103": ("bwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_fwd_sm103_paged": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_fwd_sm103_sparse": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
 }
 
 
@@ -436,9 +457,47 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError(f"device error in the timed paged prefill: {eta.attn_status_string(err)}")
         pp_ms = np.array([e0.elapsed_time(e1) for e0, e1 in p_ev])
 
+    # ---- block-sparse prefill (global + local pattern), in a loop of its own
+    bs_ms = None
+    spc = inputs.C7
+    if args.workload in ("both", "prefill") and not args.no_blocksparse:
+        sq, sk, sv, spat = inputs.sparse_config_inputs(spc, seed=spc.seed + rank)
+        srp, sci = inputs.block_csr(spat)
+        sq, sk, sv, srp, sci = sq.to(dev), sk.to(dev), sv.to(dev), srp.to(dev), sci.to(dev)
+        so = torch.empty_like(sq)
+        slse = torch.empty(sq.shape[:3], dtype=torch.float32, device=dev)
+        bs_flops = 4 * spc.d * spc.B * spc.Hq * blocksparse_pairs(spat.numpy(), spc.N, spc.N, spc.causal, -1)
+
+        def run_bs():
+            eta.attn_fwd_blocksparse(sq, sk, sv, srp, sci, causal=spc.causal, scale=spc.scale, out=so, lse=slse)
+
+        for _ in range(args.warmup):
+            run_bs()
+        torch.cuda.synchronize()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the block-sparse warm-up: {eta.attn_status_string(err)}")
+        s_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for e0, e1 in s_ev:
+            e0.record(stream)
+            run_bs()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the timed block-sparse prefill: {eta.attn_status_string(err)}")
+        bs_ms = np.array([e0.elapsed_time(e1) for e0, e1 in s_ev])
+
     # ---- max over ranks
     extra = ([float(bwd_ms.mean())] if bwd_ms is not None else []) + ([float(pp_ms.mean())] if pp_ms is not None else [])
+    extra += [float(bs_ms.mean())] if bs_ms is not None else []
     vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms + extra, world, dev)
+    bs_mean = vals.pop() if bs_ms is not None else None
     pp_mean = vals.pop() if pp_ms is not None else None
     bwd_mean = vals.pop() if bwd_ms is not None else None
     total_ms, means, e2e_ms = vals[0], vals[1:1 + len(parts)], vals[1 + len(parts):]
@@ -544,6 +603,24 @@ def run_ours(args, rank, world, local_rank):
                          "ms_per_launch": round(pp_mean, 4),
                          "ms_p10_p50_p90": [round(float(np.percentile(pp_ms, x)), 4) for x in (10, 50, 90)]},
         }
+    if bs_ms is not None:
+        achieved = bs_flops / (bs_mean * 1e-3) / 1e12
+        result["blocksparse"] = {
+            "value": round(whole_job_rate(bs_flops, world, bs_mean, 1e12), 2), "unit": "TFLOP/s",
+            "workload": spc.name, "flops_per_launch": bs_flops, "steps": args.steps, "warmup": args.warmup,
+            "gpu_launches": args.steps,
+            "config": {"B": spc.B, "Hq": spc.Hq, "Hkv": spc.Hkv, "N": spc.N, "d": spc.d, "causal": spc.causal,
+                       "global_blocks": spc.n_global, "local_blocks": spc.n_local,
+                       "listed_blocks": int(spat.sum()), "all_blocks": int(spat.numel())},
+            "roofline": {"kernel": "attn_fwd_sm103<128, sparse>", "bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "peak_kind": f"{peak_kind} bf16 dense burst",
+                         "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                         "traffic": load_traffic("attn_fwd_sm103_sparse"),
+                         "ms_per_launch": round(bs_mean, 4),
+                         "ms_p10_p50_p90": [round(float(np.percentile(bs_ms, x)), 4) for x in (10, 50, 90)]},
+        }
     return result
 
 
@@ -636,6 +713,7 @@ def main():
                     help="profiling aid: run only one half of the step (the JSON line then omits the other)")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-paged-prefill", action="store_true", help="skip the chunked paged prefill measurement")
+    ap.add_argument("--no-blocksparse", action="store_true", help="skip the block-sparse prefill measurement")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences than the workload's 64")
     args = ap.parse_args()

@@ -1,5 +1,5 @@
-"""GB300-native exact tiled attention (sm_103a): prefill (dense or over a paged cache), its
-backward, and paged GQA decode.
+"""GB300-native exact tiled attention (sm_103a): prefill (dense, block-sparse, or over a paged
+cache), its backward, and paged GQA decode.
 
 The compute lives in ``libattn.so`` (CUDA, built in-tree by ``build()``); its C ABI is
 ``include/attn.h``. ``binding`` exposes the same entry points to Python with torch
@@ -7,10 +7,10 @@ tensors as device memory. ``inputs`` holds the seeded synthetic workloads.
 """
 from .buildlib import build
 from .binding import (AttnError, attn_bwd, attn_bwd_workspace_size, attn_decode, attn_decode_chunk_tokens,
-                      attn_decode_noalloc, attn_decode_workspace_size, attn_fwd, attn_get_device_error,
+                      attn_decode_noalloc, attn_decode_workspace_size, attn_fwd, attn_fwd_blocksparse, attn_get_device_error,
                       attn_kv_layout_version, attn_prefill_paged, attn_status_string, load_library)
 
-__all__ = ["build", "AttnError", "attn_fwd", "attn_prefill_paged", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
+__all__ = ["build", "AttnError", "attn_fwd", "attn_fwd_blocksparse", "attn_prefill_paged", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
            "attn_decode_noalloc", "attn_decode_workspace_size",
            "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
            "load_library"]

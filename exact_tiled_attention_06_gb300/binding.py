@@ -24,7 +24,7 @@ STATUS_NAMES = {
 }
 
 # Every symbol include/attn.h declares.
-EXPORTED = ("attn_fwd", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
+EXPORTED = ("attn_fwd", "attn_fwd_blocksparse", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
             "attn_decode_noalloc")
 
@@ -56,6 +56,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_blocksparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, vp]
+        lib.attn_fwd_blocksparse.restype = i
         lib.attn_prefill_paged.argtypes = [vp] * 8 + [i] * 8 + [f, i, i, vp]
         lib.attn_prefill_paged.restype = i
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
@@ -137,6 +139,37 @@ def attn_fwd(q, k, v, causal=False, window=-1, scale=None, out=None, lse=None, s
                                  float(scale), int(bool(causal)), int(window), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, causal=False, window=-1, scale=None, out=None, lse=None,
+                         stream=None):
+    """Block-sparse prefill. q [B][Hq][Nq][d], k/v [B][Hkv][Nk][d] bf16; row_ptr int32
+    [ceil(Nq / 128) + 1] and col_idx int32 list the 128 x 128 blocks to visit (device)."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    _need(row_ptr, "row_ptr", torch.int32, 1)
+    _need(col_idx, "col_idx", torch.int32, 1)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if Bk != B or dk != d or v.shape != k.shape:
+        raise ValueError("q/k/v shapes disagree")
+    if row_ptr.shape[0] != (Nq + 127) // 128 + 1:
+        raise ValueError("row_ptr must have ceil(Nq / 128) + 1 entries")
+    if col_idx.numel() == 0:
+        col_idx = torch.zeros(1, dtype=torch.int32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().attn_fwd_blocksparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                             float(scale), int(bool(causal)), int(window), _ptr(row_ptr),
+                                             _ptr(col_idx), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_blocksparse")
     return out, lse
 
 

@@ -145,6 +145,34 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       static_cast<cudaStream_t>(stream), err);
 }
 
+ATTN_API int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int Nq, int Nk, int d, float scale, int causal, int window,
+                                  const int32_t* row_ptr, const int32_t* col_idx, void* stream)
+{
+    // ---- arguments (no CUDA call before these checks)
+    if (!q || !o || !lse || !row_ptr || !col_idx) return kErrInvalidArg;
+    if ((!k || !v) && Nk != 0) return kErrInvalidArg;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return kErrInvalidArg;
+    if (Hq % Hkv != 0) return kErrInvalidArg;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return kErrInvalidArg;
+    if (static_cast<long long>(B) * Hq > INT32_MAX / 2 || static_cast<long long>(B) * Hkv > INT32_MAX / 2)
+        return kErrInvalidArg;
+    if (d != 64 && d != 128) return kErrUnsupported;
+    if (Nk > kSparseMaxKeys) return kErrUnsupported;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) || !aligned4(row_ptr) ||
+        !aligned4(col_idx))
+        return kErrMisaligned;
+    if (Nq == 0) return kOk;
+    // ---- device
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc != kOk) return rc;
+    unsigned* err = device_error_word();
+    if (!err) return kErrCuda;
+    return launch_fwd_blocksparse(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, window, row_ptr, col_idx,
+                                  static_cast<cudaStream_t>(stream), err);
+}
+
 ATTN_API int attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                                 const int32_t* q_lens, const int32_t* kv_lens, void* o, float* lse, int num_seqs,
                                 int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq, int num_blocks,

@@ -30,6 +30,13 @@
 // copies each 128-key tile as min(block_size, 128)-row boxes from the cache's physical
 // blocks and skips blocks past the sequence; in the last, partial tile it zeroes the V
 // rows past the sequence (whatever the cache holds there) before P V may read them.
+//
+// MODE = sparse visits only the 128 x 128 score blocks a CSR block index lists
+// ("Modern attention kernels", "Kernel structure": an arbitrary sparse mask needs an
+// index of the blocks that exist; sparse attention visits the selected score blocks),
+// intersected element by element with the causal / window masks. The block's two query
+// tiles' lists are merged once into a shared-memory walk (key tile, tiles it is active
+// for); the producer, the MMA thread and the softmax warps all step through that walk.
 #include <climits>
 #include <cmath>
 #include <cuda_bf16.h>
@@ -48,6 +55,9 @@ constexpr int kFwdThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: move the max only if it rises by > 256x
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kModeDense = 0, kModePaged = 1, kModeSparse = 2;
+constexpr int kMaxWalk = 4096;                        // sparse: entries of the merged walk
+constexpr int kWalkBytes = kMaxWalk * 4 + 16;         // entries + {count, last entry of tile 0 / 1}
 
 template <int D>
 struct FwdCfg {
@@ -65,7 +75,7 @@ struct FwdCfg {
     static constexpr int kSmemBytes = kUsedBytes + 1024;  // slack for the 1024-byte alignment
     static constexpr uint32_t kTmemCols = 512;            // S0 | S1 | O0 | O1
     static constexpr uint32_t kOCol = 2 * BN;
-    static_assert(kUsedBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kUsedBytes + 1024 + kWalkBytes <= 227 * 1024, "shared memory budget (with the sparse walk)");
     static_assert(kOCol + 2 * D <= kTmemCols, "TMEM budget");
 };
 
@@ -77,6 +87,8 @@ struct FwdParams {
     const int32_t* q_lens;       // paged: [B] new queries per sequence (device)
     const int32_t* kv_lens;      // paged: [B] cached tokens per sequence, new ones included (device)
     int max_blocks, block_size, bs_log2, num_blocks;
+    const int32_t* row_ptr;      // sparse: [ceil(Nq / 128) + 1] CSR row offsets (device)
+    const int32_t* col_idx;      // sparse: listed key blocks, ascending per query block (device)
     float scale_log2;  // scale * log2(e)
     int causal, window;
     int pair_heads;    // 1: tiles are query heads (2u, 2u+1) at one row tile; 0: row tiles (2r, 2r+1)
@@ -136,12 +148,14 @@ __device__ __forceinline__ bool tile_active(const TileWork& t, int j)
     return t.rows > 0 && t.kv_lo <= j && j < t.kv_hi;
 }
 
-template <int D, bool PAGED>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
 {
     using C = FwdCfg<D>;
+    constexpr bool PAGED = MODE == kModePaged;
+    constexpr bool SPARSE = MODE == kModeSparse;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tw[1] = make_tile(p, hu, (2 * ru + 1) * BM, nq, nk);
     }
     const int hkv = tw[0].head / p.G;
-    const bool act[2] = {tw[0].rows > 0 && tw[0].kv_lo < tw[0].kv_hi, tw[1].rows > 0 && tw[1].kv_lo < tw[1].kv_hi};
+    bool act[2] = {tw[0].rows > 0 && tw[0].kv_lo < tw[0].kv_hi, tw[1].rows > 0 && tw[1].kv_lo < tw[1].kv_hi};
     int lo = INT_MAX, hi = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -200,7 +214,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             hi = max(hi, tw[t].kv_hi);
         }
     }
-    const bool has_work = lo < hi;
+    bool has_work = lo < hi;
 
     // ---- barriers
     const uint32_t bar0 = sb + C::kBarOff;
@@ -242,10 +256,86 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
+    // ---- sparse: merge the two query tiles' listed key blocks into the walk
+    uint32_t* walk = reinterpret_cast<uint32_t*>(smem + C::kUsedBytes);  // sparse only (kWalkBytes)
+    if constexpr (SPARSE) {
+        // the lists, copied by every thread into the (still unused) K/V ring
+        int32_t* raw = reinterpret_cast<int32_t*>(smem + C::kRingOff);
+        int beg[2] = {0, 0}, len[2] = {0, 0};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (!act[t]) continue;
+            const int qb = tw[t].row0 / BM;
+            beg[t] = p.row_ptr[qb];
+            len[t] = p.row_ptr[qb + 1] - beg[t];
+            if (len[t] < 0 || len[t] > kMaxWalk / 2) {
+                if (threadIdx.x == 0) report_error(p.err, kDevErrBounds);
+                len[t] = 0;
+            }
+        }
+        for (int e = threadIdx.x; e < len[0] + len[1]; e += kFwdThreads)
+            raw[e] = e < len[0] ? p.col_idx[beg[0] + e] : p.col_idx[beg[1] + e - len[0]];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            // entry = key tile | bit 30 + t when tile t lists it inside its causal / window
+            // range; listed tiles must ascend strictly and lie below ceil(Nk / 128)
+            const int n_kblk = (nk + BN - 1) / BN;
+            int i0 = 0, i1 = 0, n = 0, prev = -1, last0 = -1, last1 = -1;
+            while (i0 < len[0] || i1 < len[1]) {
+                const int c0 = i0 < len[0] ? raw[i0] : INT_MAX;
+                const int c1 = i1 < len[1] ? raw[len[0] + i1] : INT_MAX;
+                const int j = c0 < c1 ? c0 : c1;
+                uint32_t m = 0;
+                if (c0 == j) {
+                    ++i0;
+                    if (tw[0].kv_lo <= j && j < tw[0].kv_hi) m |= 1u;
+                }
+                if (c1 == j) {
+                    ++i1;
+                    if (tw[1].kv_lo <= j && j < tw[1].kv_hi) m |= 2u;
+                }
+                if (j < 0 || j >= n_kblk || j <= prev) {
+                    report_error(p.err, kDevErrBounds);
+                    continue;
+                }
+                prev = j;
+                if (m == 0) continue;
+                walk[4 + n] = static_cast<uint32_t>(j) | (m << 30);
+                if (m & 1u) last0 = n;
+                if (m & 2u) last1 = n;
+                ++n;
+            }
+            walk[0] = static_cast<uint32_t>(n);
+            walk[1] = static_cast<uint32_t>(last0);
+            walk[2] = static_cast<uint32_t>(last1);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+
+    // ---- key-tile walk: entry e -> key tile walk_j(e), active for query tile t when
+    // walk_act(t, e); the last entry of tile t is last_e[t]. Dense and paged: the range
+    // [lo, hi) with each tile's own band.
+    int n_walk = has_work ? hi - lo : 0;
+    int last_e[2] = {tw[0].kv_hi - 1 - lo, tw[1].kv_hi - 1 - lo};
+    if constexpr (SPARSE) {
+        n_walk = static_cast<int>(walk[0]);
+        last_e[0] = static_cast<int>(walk[1]);
+        last_e[1] = static_cast<int>(walk[2]);
+        act[0] = last_e[0] >= 0;
+        act[1] = last_e[1] >= 0;
+        has_work = n_walk > 0;
+    }
+    auto walk_j = [&](int e) -> int {
+        if constexpr (SPARSE) return static_cast<int>(walk[4 + e] & 0x3FFFFFFFu);
+        else return lo + e;
+    };
+    auto walk_act = [&](int t, int e) -> bool {
+        if constexpr (SPARSE) return ((walk[4 + e] >> (30 + t)) & 1u) != 0u;
+        else return tile_active(t ? tw[1] : tw[0], lo + e);
+    };
 
     const uint32_t sQ = sb + C::kQOff;
     const uint32_t sRing = sb + C::kRingOff;
@@ -271,7 +361,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if constexpr (!PAGED) {
             if (has_work && lane == 0) {
                 bool ok = true;
-                for (int j = lo; j < hi && ok; ++j) {
+                for (int e = 0; e < n_walk && ok; ++e) {
+                    const int j = walk_j(e);
 #pragma unroll
                     for (int kind = 0; kind < 2; ++kind) {
                         const int s = n % C::kStages;
@@ -305,11 +396,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                                   (key >> p.bs_log2))
                                           : 0;
             };
-            int ent_next = entry(lo);
+            int ent_next = entry(walk_j(0));
             bool ok = true;
-            for (int j = lo; j < hi && ok; ++j) {
+            for (int e = 0; e < n_walk && ok; ++e) {
+                const int j = walk_j(e);
                 const int ent = ent_next;
-                if (j + 1 < hi) ent_next = entry(j + 1);
+                if (e + 1 < n_walk) ent_next = entry(walk_j(e + 1));
                 const int key = j * BN + my_u * sub_rows;
                 const bool copy = mine && key < nk;
                 int row = 0;
@@ -422,52 +514,53 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (ok) {
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
-                        if (tile_active(tw[t], lo)) {
+                        if (walk_act(t, 0)) {
                             issue_qk(t, ks);
                             tc_commit(s_full(t));
                         }
                     tc_commit(kv_empty(ks));
                 }
             }
-            for (int j = lo; j < hi && ok; ++j) {
+            for (int e = 0; e < n_walk && ok; ++e) {
+                const int j = walk_j(e);
                 const int vs = n % C::kStages;
                 if (!mbar_wait(kv_full(vs), (n / C::kStages) & 1, abort_flag, p.err)) break;
                 // paged: the partial tile's V is usable once its tail rows are zeroed
                 if (PAGED && j == tail_j && !mbar_wait(bar_vtail, 0, abort_flag, p.err)) break;
                 tc_fence_after();
                 ++n;
-                const bool has_next = j + 1 < hi;
+                const bool has_next = e + 1 < n_walk;
                 const int ks = n % C::kStages;
                 // tile 0: O0 += P0 V_j, then S0 for the next key tile
-                if (tile_active(tw[0], j)) {
+                if (walk_act(0, e)) {
                     if (!mbar_wait(p_full(0), pphase[0], abort_flag, p.err)) break;
                     pphase[0] ^= 1u;
                     tc_fence_after();
                     issue_pv(0, vs, !first_pv[0]);
                     first_pv[0] = false;
-                    if (j == tw[0].kv_hi - 1) tc_commit(o_done(0));
+                    if (e == last_e[0]) tc_commit(o_done(0));
                 }
                 if (has_next) {
                     if (!mbar_wait(kv_full(ks), (n / C::kStages) & 1, abort_flag, p.err)) break;
                     tc_fence_after();
                     ++n;
-                    if (tile_active(tw[0], j + 1)) {
+                    if (walk_act(0, e + 1)) {
                         issue_qk(0, ks);
                         tc_commit(s_full(0));
                     }
                 }
                 // tile 1: O1 += P1 V_j, then S1 for the next key tile
-                if (tile_active(tw[1], j)) {
+                if (walk_act(1, e)) {
                     if (!mbar_wait(p_full(1), pphase[1], abort_flag, p.err)) break;
                     pphase[1] ^= 1u;
                     tc_fence_after();
                     issue_pv(1, vs, !first_pv[1]);
                     first_pv[1] = false;
-                    if (j == tw[1].kv_hi - 1) tc_commit(o_done(1));
+                    if (e == last_e[1]) tc_commit(o_done(1));
                 }
                 tc_commit(kv_empty(vs));
                 if (has_next) {
-                    if (tile_active(tw[1], j + 1)) {
+                    if (walk_act(1, e + 1)) {
                         issue_qk(1, ks);
                         tc_commit(s_full(1));
                     }
@@ -499,7 +592,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             long long key_max = static_cast<long long>(nk) - 1;
             if (p.causal && diag < key_max) key_max = diag;
             const long long key_min = p.window >= 0 ? diag - p.window : LLONG_MIN / 4;
-            for (int j = T.kv_lo; j < T.kv_hi; ++j) {
+            for (int e = 0; e < n_walk; ++e) {
+                bool mine;  // (warp-uniform)
+                if constexpr (SPARSE) mine = ((walk[4 + e] >> (30 + t)) & 1u) != 0u;
+                else mine = tile_active(T, lo + e);
+                if (!mine) continue;
+                const int j = walk_j(e);
                 if (!mbar_wait(s_full(t), n_act & 1, abort_flag, p.err)) {
                     ok = false;
                     break;
@@ -635,7 +733,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 template <int D>
 int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
-                 int Nk, float scale, int causal, int window, cudaStream_t stream, unsigned* err)
+                 int Nk, float scale, int causal, int window, const int32_t* row_ptr, const int32_t* col_idx,
+                 cudaStream_t stream, unsigned* err)
 {
     using C = FwdCfg<D>;
     CUtensorMap tq, tk, tv;
@@ -679,15 +778,25 @@ int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* ls
     prm.q_lens = nullptr;
     prm.kv_lens = nullptr;
     prm.max_blocks = prm.block_size = prm.bs_log2 = prm.num_blocks = 0;
+    prm.row_ptr = row_ptr;
+    prm.col_idx = col_idx;
     prm.err = err;
     const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
     if (grid > INT_MAX) return kErrInvalidArg;
 
-    if (cudaFuncSetAttribute(attn_fwd_sm103<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
+    if (row_ptr) {  // block-sparse: the walk follows the used bytes
+        if (cudaFuncSetAttribute(attn_fwd_sm103<D, kModeSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes + kWalkBytes) != cudaSuccess)
+            return kErrCuda;
+        attn_fwd_sm103<D, kModeSparse><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes + kWalkBytes, stream>>>(
+            tq, tk, tv, prm);
+        return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+    }
+    if (cudaFuncSetAttribute(attn_fwd_sm103<D, kModeDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
         return kErrCuda;
-    attn_fwd_sm103<D, false><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    attn_fwd_sm103<D, kModeDense><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 
@@ -734,6 +843,8 @@ int launch_fwd_paged_d(const void* q, const void* k_cache, const void* v_cache, 
     prm.block_size = block_size;
     prm.bs_log2 = 31 - __builtin_clz(static_cast<unsigned>(block_size));
     prm.num_blocks = num_blocks;
+    prm.row_ptr = nullptr;
+    prm.col_idx = nullptr;
     prm.scale_log2 = scale * kLog2e;
     prm.causal = causal ? 1 : 0;
     prm.window = window < 0 ? -1 : window;
@@ -745,10 +856,10 @@ int launch_fwd_paged_d(const void* q, const void* k_cache, const void* v_cache, 
     const long long grid = static_cast<long long>(S) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
     if (grid > INT_MAX) return kErrInvalidArg;
-    if (cudaFuncSetAttribute(attn_fwd_sm103<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(attn_fwd_sm103<D, kModePaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
         return kErrCuda;
-    attn_fwd_sm103<D, true><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    attn_fwd_sm103<D, kModePaged><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 
@@ -758,8 +869,26 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nk, int d, float scale, int causal, int window, cudaStream_t stream, unsigned* err)
 {
     if (Nq == 0) return kOk;
-    if (d == 128) return launch_fwd_d<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream, err);
-    if (d == 64) return launch_fwd_d<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream, err);
+    if (d == 128)
+        return launch_fwd_d<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, nullptr, nullptr, stream,
+                                 err);
+    if (d == 64)
+        return launch_fwd_d<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, nullptr, nullptr, stream,
+                                err);
+    return kErrUnsupported;
+}
+
+int launch_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int d, float scale, int causal, int window, const int32_t* row_ptr,
+                           const int32_t* col_idx, cudaStream_t stream, unsigned* err)
+{
+    if (Nq == 0) return kOk;
+    if (d == 128)
+        return launch_fwd_d<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, row_ptr, col_idx, stream,
+                                 err);
+    if (d == 64)
+        return launch_fwd_d<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, row_ptr, col_idx, stream,
+                                err);
     return kErrUnsupported;
 }
 

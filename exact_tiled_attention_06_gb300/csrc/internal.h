@@ -41,6 +41,13 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nq, int Nk, int d, float scale, int causal, int window, cudaStream_t stream,
                unsigned* err);
 
+// Block-sparse prefill (implemented in fwd_kernel.cu): 128 x 128 blocks listed in CSR form
+// (row_ptr [ceil(Nq / 128) + 1], col_idx), device pointers. Arguments are already validated.
+constexpr int kSparseMaxKeys = 2048 * 128;  // the merged walk holds 4096 entries
+int launch_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                           int Nq, int Nk, int d, float scale, int causal, int window, const int32_t* row_ptr,
+                           const int32_t* col_idx, cudaStream_t stream, unsigned* err);
+
 // Paged prefill (implemented in fwd_kernel.cu). Arguments are already validated.
 int launch_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                      const int32_t* q_lens, const int32_t* kv_lens, void* o, float* lse, int S, int Hq, int Hkv, int d,

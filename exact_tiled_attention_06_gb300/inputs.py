@@ -16,6 +16,10 @@ Recipe (one ``torch.Generator`` on the CPU per call, seeded explicitly):
   iid N(0, 1) rounded to bf16. The block table lists each sequence's physical
   blocks in logical order; unused entries are -1. ``poison`` fills every cache
   slot that no sequence owns (tail slots of a last block, unused blocks) with NaN.
+* block-sparse prefill: the prefill recipe for q, k, v; the block index is either
+  a global + local pattern (every query block lists the first ``n_global`` key
+  blocks and the ``n_local`` blocks ending at its diagonal block) or a seeded
+  random pattern, stored as CSR (row_ptr, col_idx).
 * paged prefill: the cache and table of the decode recipe for the sequences'
   kv lengths (query lengths drawn first when not given), then q [S][Hq][max_q][d]
   from a generator seeded apart; ``poison`` also fills q rows past each q_len with NaN.
@@ -103,7 +107,30 @@ C5 = DecodeConfig("C5_paged_gqa_decode_S64_Hq32_Hkv8_d128_bs16_L1k_32k", 64, 32,
 C6 = PagedPrefillConfig("C6_chunked_prefill_paged_S16_q2048_ctx0_14k_Hq32_Hkv8_d128_bs16", 16, 32, 8, 128, 16,
                         2048, 0, 14336)
 
+@dataclass(frozen=True)
+class SparsePrefillConfig:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    N: int
+    d: int
+    causal: bool
+    n_global: int   # key blocks every query block lists (from the start)
+    n_local: int    # key blocks ending at the query block's diagonal block
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# Long-context block-sparse prefill with a global + local pattern (the pages name the
+# pattern, not a size): 32k tokens, one global key block and an 8-block local band.
+C7 = SparsePrefillConfig("C7_blocksparse_global1_local8_B1_H32_N32768_d128_causal", 1, 32, 32, 32768, 128, True, 1, 8)
+
 PREFILL_CONFIGS = {c.name: c for c in (C1, C2, C3, C4)}
+SPARSE_CONFIGS = {C7.name: C7}
 PAGED_PREFILL_CONFIGS = {C6.name: C6}
 DECODE_CONFIGS = {C5.name: C5}
 
@@ -251,3 +278,43 @@ def paged_prefill_config_inputs(cfg: PagedPrefillConfig, seed=None):
     q_lens = [cfg.q_len] * cfg.num_seqs
     kv_lens = [int(c) + cfg.q_len for c in ctx]
     return paged_prefill_inputs(cfg.num_seqs, cfg.Hq, cfg.Hkv, cfg.d, cfg.block_size, q_lens, kv_lens, seed=sd)
+
+
+def block_csr(pattern):
+    """Boolean block pattern [n_qblk][n_kblk] -> CSR (row_ptr, col_idx) as int32 tensors."""
+    pat = torch.as_tensor(pattern, dtype=torch.bool)
+    counts = pat.sum(dim=1).to(torch.int64)
+    row_ptr = torch.zeros(pat.shape[0] + 1, dtype=torch.int64)
+    row_ptr[1:] = torch.cumsum(counts, dim=0)
+    col_idx = torch.nonzero(pat, as_tuple=False)[:, 1]
+    return row_ptr.to(torch.int32), col_idx.to(torch.int32)
+
+
+def global_local_pattern(n_qblk, n_kblk, n_global, n_local):
+    """Every query block r lists key blocks [0, n_global) and the n_local blocks ending at its
+    diagonal block r + (n_kblk - n_qblk) (bottom-right alignment), clipped to the key range."""
+    pat = torch.zeros((n_qblk, n_kblk), dtype=torch.bool)
+    for r in range(n_qblk):
+        diag = r + (n_kblk - n_qblk)
+        pat[r, :max(0, min(n_global, n_kblk))] = True
+        lo, hi = max(0, diag - n_local + 1), min(n_kblk, diag + 1)
+        if hi > lo:
+            pat[r, lo:hi] = True
+    return pat
+
+
+def random_pattern(n_qblk, n_kblk, density, seed=0, empty_rows=()):
+    """Seeded random block pattern; rows in ``empty_rows`` list nothing."""
+    gen = torch.Generator().manual_seed(int(seed))
+    pat = torch.rand((n_qblk, n_kblk), generator=gen) < density
+    for r in empty_rows:
+        pat[r] = False
+    return pat
+
+
+def sparse_config_inputs(cfg: SparsePrefillConfig, seed=None):
+    """q, k, v of the block-sparse workload and its global + local pattern."""
+    q, k, v = prefill_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d, seed=cfg.seed if seed is None else seed)
+    nb = (cfg.N + 127) // 128
+    pat = global_local_pattern(nb, nb, cfg.n_global, cfg.n_local)
+    return q, k, v, pat

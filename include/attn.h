@@ -73,6 +73,32 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int causal, int window, void* stream);
 
 /*
+ * attn_fwd_blocksparse -- prefill restricted to the 128 x 128 score blocks a block index
+ * lists.
+ *
+ *   MAK "Kernel structure" (an arbitrary sparse mask needs an index structure telling the
+ *   kernel which blocks exist; tiles that do not exist are never visited); MAK, the table
+ *   of attention variants (sparse attention visits selected score blocks); AK, sparse
+ *   attention (global plus local patterns keep softmax attention and restrict positions).
+ *
+ *   q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale: as attn_fwd.
+ *   row_ptr : int32 [ceil(Nq / 128) + 1] (device) CSR offsets into col_idx, row_ptr[0] = 0
+ *   col_idx : int32 [row_ptr[last]] (device) key blocks (keys [128 c, 128 c + 128)) listed
+ *             for each query block (rows [128 r, 128 r + 128)), strictly ascending, each
+ *             below ceil(Nk / 128); one index serves every batch entry and head.
+ *   causal, window: as attn_fwd, applied element by element inside the listed blocks.
+ *   Row i attends key j when block (i / 128, j / 128) is listed and the causal / window
+ *   mask allows (i, j); a row with no such key gets O = 0 and lse = -inf.
+ *   Nk <= 262144 and at most 2048 blocks per query block. An entry out of range or out of
+ *   order sets ATTN_ERR_DEVICE_BOUNDS in the device error word and is skipped.
+ *   Enqueues one kernel on `stream`. Returns ATTN_OK or a negative attn_status.
+ */
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                         int causal, int window, const int32_t* row_ptr, const int32_t* col_idx,
+                         void* stream);
+
+/*
  * attn_prefill_paged -- prefill of several sequences against a paged KV cache (chunked
  * prefill): each sequence's new queries attend to its cached tokens, the new ones included.
  *

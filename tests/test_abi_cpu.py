@@ -104,6 +104,24 @@ def test_bwd_workspace_size(lib):
     assert eta.attn_bwd_workspace_size(0, 4, 200, 64) == 0
 
 
+def bsp(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=1, Nq=300, Nk=300, d=64, scale=0.125, causal=1,
+        window=-1, rp=FAKE, ci=FAKE):
+    return lib.attn_fwd_blocksparse(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, window, rp, ci, None)
+
+
+def test_fwd_blocksparse_argument_validation(lib):
+    assert bsp(lib, rp=None) == -1
+    assert bsp(lib, ci=None) == -1
+    assert bsp(lib, q=None) == -1
+    assert bsp(lib, Hq=3, Hkv=2) == -1
+    assert bsp(lib, scale=-0.5) == -1
+    assert bsp(lib, d=80) == -2
+    assert bsp(lib, Nk=262145) == -2          # the merged walk holds 2048 key blocks per tile
+    assert bsp(lib, rp=FAKE + 2) == -3
+    assert bsp(lib, o=FAKE + 4) == -3
+    assert bsp(lib, Nq=0) == 0
+
+
 def ppf(lib, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, ql=FAKE, kl=FAKE, o=FAKE, lse=FAKE, S=4, Hq=8, Hkv=2, d=128, bs=16,
         mb=64, nb=256, max_q=300, scale=0.1, causal=1, window=-1):
     return lib.attn_prefill_paged(q, kc, vc, bt, ql, kl, o, lse, S, Hq, Hkv, d, bs, mb, nb, max_q, scale, causal,

@@ -2,6 +2,8 @@
 import json
 import os
 
+import numpy as np
+
 import bench
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "page_figures.json")
@@ -62,3 +64,14 @@ def test_paged_prefill_flops():
     # a whole prompt (q_len = kv_len) equals causal prefill; one query sees every key
     assert bench.paged_prefill_flops([300], [300], 4, 64, True) == bench.attention_flops(1, 4, 300, 300, 64, True)
     assert bench.paged_prefill_flops([1], [77], 1, 64, True) == 4 * 64 * 77
+
+
+def test_blocksparse_pairs():
+    """A full pattern counts the dense mask's pairs; a block-diagonal one counts the blocks."""
+    for Nq, Nk, causal, window in ((300, 300, True, -1), (200, 450, True, 100), (257, 129, False, -1)):
+        nq, nk = -(-Nq // 128), -(-Nk // 128)
+        full = np.ones((nq, nk), dtype=bool)
+        assert bench.blocksparse_pairs(full, Nq, Nk, causal, window) == bench.allowed_pairs(Nq, Nk, causal, window)
+    eye = np.eye(3, dtype=bool)
+    assert bench.blocksparse_pairs(eye, 384, 384, False, -1) == 3 * 128 * 128
+    assert bench.blocksparse_pairs(eye, 384, 384, True, -1) == 3 * 128 * 129 // 2
