@@ -15,6 +15,10 @@ attn_prefill_paged on the chunked-prefill workload (16 sequences, 2048 new queri
 each over a paged cache) the same way; ``--no-paged-prefill`` skips it. ``blocksparse``
 times attn_fwd_blocksparse on a 32k-token global + local block pattern the same way
 (4 * d FLOPs per allowed pair of the listed blocks); ``--no-blocksparse`` skips it.
+``decode_graph`` times a 32-layer decode step (8 sequences, each layer its own cache) two
+ways: one attn_decode call per layer, and the same calls captured once with
+attn_decode_graph_create and replayed with one graph launch per step (KV GB/s over the
+step); ``--no-decode-graph`` skips it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -382,6 +386,31 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = [float(np.mean([e_ev[i][j][0].elapsed_time(e_ev[i][j][1]) for i in range(e2e_steps)]))
                   for j in range(len(parts))]
 
+    def timed_loop(run, what):
+        """W untimed calls, then K calls each bracketed by CUDA events on the launching
+        stream, between barriers; the device error word is checked after both."""
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the {what} warm-up: {eta.attn_status_string(err)}")
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            e0.record(stream)
+            run()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        err = eta.attn_get_device_error()
+        if err != 0:
+            raise RuntimeError(f"device error in the timed {what}: {eta.attn_status_string(err)}")
+        return np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+
     # ---- backward of the prefill workload, in a loop of its own: W untimed launches,
     #      then K launches bracketed by CUDA events on the launching stream (inputs and
     #      the fp32 dQ accumulator exceed L2, so no flush is needed)
@@ -399,27 +428,7 @@ def run_ours(args, rank, world, local_rank):
             eta.attn_bwd(pre.dev["q"], pre.dev["k"], pre.dev["v"], o, do_d, lse, causal=pc.causal,
                          window=pc.window, scale=pc.scale, workspace=ws_b, dq=dq, dk=dk, dv=dv)
 
-        for _ in range(args.warmup):
-            run_bwd()
-        torch.cuda.synchronize()
-        err = eta.attn_get_device_error()
-        if err != 0:
-            raise RuntimeError(f"device error in the backward warm-up: {eta.attn_status_string(err)}")
-        b_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for e0, e1 in b_ev:
-            e0.record(stream)
-            run_bwd()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        err = eta.attn_get_device_error()
-        if err != 0:
-            raise RuntimeError(f"device error in the timed backward: {eta.attn_status_string(err)}")
-        bwd_ms = np.array([e0.elapsed_time(e1) for e0, e1 in b_ev])
+        bwd_ms = timed_loop(run_bwd, "backward")
 
     # ---- chunked prefill over a paged cache, in a loop of its own (inputs exceed L2)
     pp_ms = None
@@ -435,27 +444,7 @@ def run_ours(args, rank, world, local_rank):
         def run_pp():
             eta.attn_prefill_paged(pq, pkc, pvc, pbt, pql, pkl, causal=ppc.causal, scale=ppc.scale, out=po, lse=plse)
 
-        for _ in range(args.warmup):
-            run_pp()
-        torch.cuda.synchronize()
-        err = eta.attn_get_device_error()
-        if err != 0:
-            raise RuntimeError(f"device error in the paged prefill warm-up: {eta.attn_status_string(err)}")
-        p_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for e0, e1 in p_ev:
-            e0.record(stream)
-            run_pp()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        err = eta.attn_get_device_error()
-        if err != 0:
-            raise RuntimeError(f"device error in the timed paged prefill: {eta.attn_status_string(err)}")
-        pp_ms = np.array([e0.elapsed_time(e1) for e0, e1 in p_ev])
+        pp_ms = timed_loop(run_pp, "paged prefill")
 
     # ---- block-sparse prefill (global + local pattern), in a loop of its own
     bs_ms = None
@@ -471,32 +460,44 @@ def run_ours(args, rank, world, local_rank):
         def run_bs():
             eta.attn_fwd_blocksparse(sq, sk, sv, srp, sci, causal=spc.causal, scale=spc.scale, out=so, lse=slse)
 
-        for _ in range(args.warmup):
-            run_bs()
-        torch.cuda.synchronize()
-        err = eta.attn_get_device_error()
-        if err != 0:
-            raise RuntimeError(f"device error in the block-sparse warm-up: {eta.attn_status_string(err)}")
-        s_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for e0, e1 in s_ev:
-            e0.record(stream)
-            run_bs()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        err = eta.attn_get_device_error()
-        if err != 0:
-            raise RuntimeError(f"device error in the timed block-sparse prefill: {eta.attn_status_string(err)}")
-        bs_ms = np.array([e0.elapsed_time(e1) for e0, e1 in s_ev])
+        bs_ms = timed_loop(run_bs, "block-sparse prefill")
+
+    # ---- a many-layer decode step (every layer its own cache): one attn_decode call per
+    #      layer from the host, against the same calls captured once as a CUDA graph and
+    #      replayed with one launch per step (the step's KV, ~1 GB, exceeds L2)
+    eager_ms = graph_ms = None
+    gc = inputs.C8
+    if args.workload in ("both", "decode") and not args.no_decode_graph:
+        gx = inputs.decode_step_config_inputs(gc, seed=gc.seed + rank)
+        gq, gk, gv = ([t.to(dev) for t in ts] for ts in (gx.q, gx.k_cache, gx.v_cache))
+        gbt, gsl = gx.block_table.to(dev), gx.seq_lens.to(dev)
+        gws = torch.empty(eta.attn_decode_workspace_size(gc.num_seqs, gc.Hq, gc.Hkv, gc.d, gc.block_size,
+                                                         gbt.shape[1]), dtype=torch.uint8, device=dev)
+        gout = [torch.empty_like(t) for t in gq]
+        glse = [torch.empty((gc.num_seqs, gc.Hq), dtype=torch.float32, device=dev) for _ in gq]
+        graph = eta.attn_decode_graph_create(gq, gk, gv, gbt, gsl, scale=gc.scale, workspace=gws, outs=gout,
+                                             lses=glse)
+        g_kv = gc.n_layers * decode_kv_bytes(gx.seq_lens.numpy(), gc.Hkv, gc.d)
+
+        def run_eager():
+            for l in range(gc.n_layers):
+                eta.attn_decode(gq[l], gk[l], gv[l], gbt, gsl, scale=gc.scale, workspace=gws, out=gout[l],
+                                lse=glse[l])
+
+        def run_graph():
+            graph.launch(stream)
+
+        eager_ms = timed_loop(run_eager, "per-call decode step")
+        graph_ms = timed_loop(run_graph, "graph decode step")
+        graph.close()
 
     # ---- max over ranks
     extra = ([float(bwd_ms.mean())] if bwd_ms is not None else []) + ([float(pp_ms.mean())] if pp_ms is not None else [])
     extra += [float(bs_ms.mean())] if bs_ms is not None else []
+    extra += [float(eager_ms.mean()), float(graph_ms.mean())] if graph_ms is not None else []
     vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms + extra, world, dev)
+    graph_mean = vals.pop() if graph_ms is not None else None
+    eager_mean = vals.pop() if graph_ms is not None else None
     bs_mean = vals.pop() if bs_ms is not None else None
     pp_mean = vals.pop() if pp_ms is not None else None
     bwd_mean = vals.pop() if bwd_ms is not None else None
@@ -621,6 +622,23 @@ def run_ours(args, rank, world, local_rank):
                          "ms_per_launch": round(bs_mean, 4),
                          "ms_p10_p50_p90": [round(float(np.percentile(bs_ms, x)), 4) for x in (10, 50, 90)]},
         }
+    if graph_ms is not None:
+        achieved = g_kv / (graph_mean * 1e-3) / 1e9
+        result["decode_graph"] = {
+            "value": round(whole_job_rate(g_kv, world, graph_mean, 1e9), 2), "unit": "GB/s",
+            "workload": gc.name, "kv_bytes_per_step": g_kv, "steps": args.steps, "warmup": args.warmup,
+            "gpu_launches": gc.n_layers * args.steps, "graph_nodes_per_step": 2 * gc.n_layers,
+            "us_per_step_graph": round(graph_mean * 1e3, 2), "us_per_step_per_call": round(eager_mean * 1e3, 2),
+            "per_call_value": round(whole_job_rate(g_kv, world, eager_mean, 1e9), 2),
+            "graph_speedup": round(eager_mean / graph_mean, 3),
+            "config": {"n_layers": gc.n_layers, "num_seqs": gc.num_seqs, "Hq": gc.Hq, "Hkv": gc.Hkv, "d": gc.d,
+                       "block_size": gc.block_size, "seq_lens": gx.seq_lens.tolist()},
+            "roofline": {"kernel": "attn_decode_sm103<128> (x n_layers, one graph)", "bound": "hbm",
+                         "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} HBM copy",
+                         "traffic": None, "ms_per_step": round(graph_mean, 4),
+                         "ms_p10_p50_p90": [round(float(np.percentile(graph_ms, x)), 4) for x in (10, 50, 90)]},
+        }
     return result
 
 
@@ -713,6 +731,8 @@ def main():
                     help="profiling aid: run only one half of the step (the JSON line then omits the other)")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-paged-prefill", action="store_true", help="skip the chunked paged prefill measurement")
+    ap.add_argument("--no-decode-graph", action="store_true",
+                    help="skip the many-layer decode step (per-call launches against one CUDA-graph replay)")
     ap.add_argument("--no-blocksparse", action="store_true", help="skip the block-sparse prefill measurement")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences than the workload's 64")

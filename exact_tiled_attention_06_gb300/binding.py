@@ -26,7 +26,8 @@ STATUS_NAMES = {
 # Every symbol include/attn.h declares.
 EXPORTED = ("attn_fwd", "attn_fwd_blocksparse", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
-            "attn_decode_noalloc")
+            "attn_decode_noalloc", "attn_decode_graph_create", "attn_decode_graph_launch", "attn_decode_graph_layers",
+            "attn_decode_graph_destroy")
 
 
 class AttnError(RuntimeError):
@@ -68,7 +69,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_decode_workspace_size.restype = sz
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.attn_decode.restype = i
-        lib.attn_decode_chunk_tokens.argtypes = [i, i, i, i]
+        lib.attn_decode_chunk_tokens.argtypes = [i, i, i, i, i]
         lib.attn_decode_chunk_tokens.restype = i
         lib.attn_get_device_error.argtypes = [vp]
         lib.attn_get_device_error.restype = i
@@ -76,6 +77,15 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_kv_layout_version.restype = i
         lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
         lib.attn_decode_noalloc.restype = i
+        lib.attn_decode_graph_create.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz,
+                                                 ctypes.POINTER(vp)]
+        lib.attn_decode_graph_create.restype = i
+        lib.attn_decode_graph_launch.argtypes = [vp, vp]
+        lib.attn_decode_graph_launch.restype = i
+        lib.attn_decode_graph_layers.argtypes = [vp]
+        lib.attn_decode_graph_layers.restype = i
+        lib.attn_decode_graph_destroy.argtypes = [vp]
+        lib.attn_decode_graph_destroy.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -245,8 +255,8 @@ def attn_decode_workspace_size(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_
     return int(load_library().attn_decode_workspace_size(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_seq))
 
 
-def attn_decode_chunk_tokens(num_seqs, Hkv, block_size, max_blocks_per_seq) -> int:
-    return int(load_library().attn_decode_chunk_tokens(num_seqs, Hkv, block_size, max_blocks_per_seq))
+def attn_decode_chunk_tokens(num_seqs, Hq, Hkv, block_size, max_blocks_per_seq) -> int:
+    return int(load_library().attn_decode_chunk_tokens(num_seqs, Hq, Hkv, block_size, max_blocks_per_seq))
 
 
 def attn_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, workspace=None, out=None, lse=None,
@@ -307,3 +317,88 @@ def attn_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=None, 
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_noalloc")
     return out, lse
+
+
+class DecodeGraph:
+    """A decode step over several layers captured once by ``attn_decode_graph_create`` and
+    replayed by ``launch()`` (one graph launch per step). The object keeps references to
+    every tensor the graph points at, so they stay alive and in place; rewrite their
+    contents (queries, cache rows, block table, lengths) between launches."""
+
+    def __init__(self, handle: int, tensors, outs, lses):
+        self._handle = handle
+        self._tensors = tensors
+        self.out = outs
+        self.lse = lses
+
+    @property
+    def layers(self) -> int:
+        return int(load_library().attn_decode_graph_layers(self._handle)) if self._handle else 0
+
+    def launch(self, stream=None):
+        if not self._handle:
+            raise RuntimeError("DecodeGraph is closed")
+        rc = load_library().attn_decode_graph_launch(self._handle, _stream_handle(stream))
+        if rc != ATTN_OK:
+            raise AttnError(rc, "attn_decode_graph_launch")
+        return self.out, self.lse
+
+    def close(self):
+        """Release the graph (synchronise any stream it was launched on first)."""
+        if self._handle:
+            h, self._handle = self._handle, None
+            rc = load_library().attn_decode_graph_destroy(h)
+            if rc != ATTN_OK:
+                raise AttnError(rc, "attn_decode_graph_destroy")
+
+    def __del__(self):
+        try:
+            if self._handle:
+                torch.cuda.synchronize()
+                self.close()
+        except Exception:
+            pass
+
+
+def attn_decode_graph_create(qs, k_caches, v_caches, block_table, seq_lens, scale=None, workspace=None,
+                             outs=None, lses=None) -> DecodeGraph:
+    """Capture one decode call per layer (attn_decode's shapes; per-layer q, caches and
+    outputs, one shared block table and seq_lens) into a CUDA graph. Returns a
+    ``DecodeGraph`` whose ``launch()`` replays the step; ``out``/``lse`` hold the
+    per-layer outputs it writes."""
+    n = len(qs)
+    if n == 0 or len(k_caches) != n or len(v_caches) != n:
+        raise ValueError("one q, k_cache and v_cache per layer")
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    S, Hq, d = qs[0].shape
+    nb, Hkv, bs, _ = k_caches[0].shape
+    for l in range(n):
+        _need(qs[l], f"q[{l}]", torch.bfloat16, 3)
+        _need(k_caches[l], f"k_cache[{l}]", torch.bfloat16, 4)
+        _need(v_caches[l], f"v_cache[{l}]", torch.bfloat16, 4)
+        if qs[l].shape != (S, Hq, d) or k_caches[l].shape != (nb, Hkv, bs, d) or v_caches[l].shape != (nb, Hkv, bs, d):
+            raise ValueError(f"layer {l}: shapes differ from layer 0")
+    if block_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("decode shapes disagree")
+    mb = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qs[0].device)
+    if outs is None:
+        outs = [torch.empty_like(qs[0]) for _ in range(n)]
+    if lses is None:
+        lses = [torch.empty((S, Hq), dtype=torch.float32, device=qs[0].device) for _ in range(n)]
+    arr = ctypes.c_void_p * n
+    h = ctypes.c_void_p()
+    rc = load_library().attn_decode_graph_create(
+        n, arr(*[t.data_ptr() for t in qs]), arr(*[t.data_ptr() for t in k_caches]),
+        arr(*[t.data_ptr() for t in v_caches]), arr(*[t.data_ptr() for t in outs]), arr(*[t.data_ptr() for t in lses]),
+        _ptr(block_table), _ptr(seq_lens), S, Hq, Hkv, d, bs, mb, nb, float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), ctypes.byref(h))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_graph_create")
+    return DecodeGraph(h.value, (list(qs), list(k_caches), list(v_caches), block_table, seq_lens, workspace),
+                       outs, lses)

@@ -32,6 +32,8 @@ bool g_encode_tried = false;
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+}  // namespace
+
 // Compute capability 10.3 (GB300) is the only target this library is built for.
 int check_device(int* dev_out)
 {
@@ -49,8 +51,6 @@ int check_device(int* dev_out)
     }
     return g_arch_ok[dev] == 1 ? kOk : kErrUnsupported;
 }
-
-}  // namespace
 
 unsigned* device_error_word()
 {
@@ -250,10 +250,10 @@ ATTN_API size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d,
     return plan.bytes;
 }
 
-ATTN_API int attn_decode_chunk_tokens(int num_seqs, int Hkv, int block_size, int max_blocks_per_seq)
+ATTN_API int attn_decode_chunk_tokens(int num_seqs, int Hq, int Hkv, int block_size, int max_blocks_per_seq)
 {
     DecodePlan plan;
-    if (!decode_plan(num_seqs, Hkv, Hkv, 128, block_size, max_blocks_per_seq, &plan)) return 0;
+    if (!decode_plan(num_seqs, Hq, Hkv, 128, block_size, max_blocks_per_seq, &plan)) return 0;
     return plan.chunk;
 }
 

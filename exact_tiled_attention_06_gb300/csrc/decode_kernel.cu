@@ -1,8 +1,8 @@
 // decode_kernel.cu -- one-query-per-sequence attention over a paged KV cache, sm_103a.
 //
 // One persistent kernel, one block per SM, eight independent worker warps per block.
-// A work item is (key chunk of 512 tokens, kv head [, group of 16 query heads],
-// sequence). Each warp repeatedly:
+// A work item is (key chunk of 512 tokens -- fewer for a small batch, down to 128 -- kv
+// head [, group of 16 query heads], sequence). Each warp repeatedly:
 //   * takes the next item from a device-wide counter (items in split-major order;
 //     chunks that lie past their sequence's end are skipped on the device, so the
 //     host never reads the sequence lengths),
@@ -40,7 +40,9 @@ namespace {
 
 constexpr int kDecWarps = 8;          // independent worker warps per block
 constexpr int kSub = 16;              // tokens per sub-page (one TMA box height)
-constexpr int kChunkTokens = 512;     // keys per work item
+constexpr int kChunkTokens = 512;     // keys per work item (the most)
+constexpr int kMinChunkTokens = 128;  // keys per work item (the fewest the planner goes down to)
+constexpr long long kTargetItems = 152 * 8;  // worker warps of a full GB300 (152 SMs x 8)
 constexpr int kMaxChunkBlocks = 32;   // block-table entries per item (one per lane)
 constexpr int kRowsPerItem = 16;      // query heads per item (mma M)
 constexpr float kRescaleThreshold = 8.0f;
@@ -354,31 +356,83 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         if (lane == 0) last = atomicAdd(p.done + static_cast<size_t>(seq) * p.HG + hg, 1) == n_splits - 1;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (!last) continue;
-        // ---- this warp finished the last chunk of (seq, head group): merge every partial
+        // ---- this warp finished the last chunk of (seq, head group): merge every partial.
+        // Eight lanes per query head (four heads at a time), each lane owning D/8
+        // consecutive columns: the log-sums of a head are reduced over its eight lanes, and
+        // the partial rows are read four chunks at a time with independent 16-byte loads,
+        // so that many loads are in flight instead of one chain per chunk.
         __threadfence();
-        for (int row = 0; row < nvalid; ++row) {
-            const size_t r0 = static_cast<size_t>(seq) * p.Hq + hq0 + row;  // row index within a split
-            const size_t split_stride = static_cast<size_t>(p.num_seqs) * p.Hq;
-            float M = -INFINITY;
-            for (int c = lane; c < n_splits; c += 32) M = fmaxf(M, __ldcg(p.part_lse + c * split_stride + r0));
+        {
+            constexpr int kCols = D / 8;           // columns per lane (16 or 8)
+            constexpr int kVec = kCols / 4;        // float4 loads per lane per chunk
+            const int slot_row = lane >> 3;        // head within the group of four
+            const int cg = lane & 7;               // column group
+            const size_t split_stride = static_cast<size_t>(p.num_seqs) * p.Hq;  // rows per chunk
+            for (int rb = 0; rb < nvalid; rb += 4) {
+                const int row = rb + slot_row;
+                const bool live = row < nvalid;
+                const size_t r0 = static_cast<size_t>(seq) * p.Hq + hq0 + (live ? row : nvalid - 1);
+                const float* lse_r = p.part_lse + r0;
+                float M = -INFINITY;
+                for (int c = cg; c < n_splits; c += 8) M = fmaxf(M, __ldcg(lse_r + c * split_stride));
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+                float S = 0.0f;
+                for (int c = cg; c < n_splits; c += 8) S += ex2_approx(__ldcg(lse_r + c * split_stride) - M);
+                S += __shfl_xor_sync(0xffffffffu, S, 1);
+                S += __shfl_xor_sync(0xffffffffu, S, 2);
+                S += __shfl_xor_sync(0xffffffffu, S, 4);
+                float acc[kCols];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float S = 0.0f;
-            float acc[D / 32];
+                for (int t = 0; t < kCols; ++t) acc[t] = 0.0f;
+                const float* po = p.part_o + r0 * D + cg * kCols;
+                int c = 0;
+                for (; c + 4 <= n_splits; c += 4) {
+                    float lv[4];
+                    float4 v[4][kVec];
 #pragma unroll
-            for (int i = 0; i < D / 32; ++i) acc[i] = 0.0f;
-            for (int c = 0; c < n_splits; ++c) {
-                const float w = ex2_approx(__ldcg(p.part_lse + c * split_stride + r0) - M);
-                S += w;
-                const float* po = p.part_o + (c * split_stride + r0) * D;
+                    for (int k = 0; k < 4; ++k) {
+                        lv[k] = __ldcg(lse_r + (c + k) * split_stride);
 #pragma unroll
-                for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(w, __ldcg(po + lane + 32 * i), acc[i]);
+                        for (int x = 0; x < kVec; ++x)
+                            v[k][x] = __ldcg(reinterpret_cast<const float4*>(po + (c + k) * split_stride * D) + x);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float w = ex2_approx(lv[k] - M);
+#pragma unroll
+                        for (int x = 0; x < kVec; ++x) {
+                            acc[4 * x + 0] = fmaf(w, v[k][x].x, acc[4 * x + 0]);
+                            acc[4 * x + 1] = fmaf(w, v[k][x].y, acc[4 * x + 1]);
+                            acc[4 * x + 2] = fmaf(w, v[k][x].z, acc[4 * x + 2]);
+                            acc[4 * x + 3] = fmaf(w, v[k][x].w, acc[4 * x + 3]);
+                        }
+                    }
+                }
+                for (; c < n_splits; ++c) {
+                    const float w = ex2_approx(__ldcg(lse_r + c * split_stride) - M);
+#pragma unroll
+                    for (int x = 0; x < kVec; ++x) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(po + c * split_stride * D) + x);
+                        acc[4 * x + 0] = fmaf(w, v.x, acc[4 * x + 0]);
+                        acc[4 * x + 1] = fmaf(w, v.y, acc[4 * x + 1]);
+                        acc[4 * x + 2] = fmaf(w, v.z, acc[4 * x + 2]);
+                        acc[4 * x + 3] = fmaf(w, v.w, acc[4 * x + 3]);
+                    }
+                }
+                if (live) {
+                    const float inv = 1.0f / S;
+                    uint4* orow = reinterpret_cast<uint4*>(p.o + r0 * D + cg * kCols);
+#pragma unroll
+                    for (int x = 0; x < kCols / 8; ++x)
+                        orow[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv, acc[8 * x + 1] * inv),
+                                             pack_bf16x2(acc[8 * x + 2] * inv, acc[8 * x + 3] * inv),
+                                             pack_bf16x2(acc[8 * x + 4] * inv, acc[8 * x + 5] * inv),
+                                             pack_bf16x2(acc[8 * x + 6] * inv, acc[8 * x + 7] * inv));
+                    if (cg == 0) p.lse[r0] = (M + log2f(S)) * kLn2;
+                }
             }
-            const float inv = 1.0f / S;
-            __nv_bfloat16* orow = p.o + r0 * D;
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
-            if (lane == 0) p.lse[r0] = (M + log2f(S)) * kLn2;
         }
     }
 }
@@ -464,13 +518,21 @@ bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_b
     chunk = (chunk / block_size) * block_size;
     if (chunk / block_size > kMaxChunkBlocks) chunk = kMaxChunkBlocks * block_size;
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
-    const long long n_split = (max_ctx + chunk - 1) / chunk;
-    if (n_split > 65535) return false;
     const int G = Hq / Hkv;
-    plan->chunk = chunk;
-    plan->n_split_max = static_cast<int>(n_split);
     plan->n_hgroups = (G + kRowsPerItem - 1) / kRowsPerItem;
     const size_t hg = static_cast<size_t>(Hkv) * plan->n_hgroups;
+    // A small batch (few, short sequences) gives fewer items than there are worker warps,
+    // and a warp streams one item at a time: halve the chunk until the items cover the
+    // warps, so that the cache reads spread over the whole GPU (more, smaller partials).
+    long long n_split = (max_ctx + chunk - 1) / chunk;
+    while (n_split * num_seqs * static_cast<long long>(hg) < kTargetItems && chunk / 2 >= kMinChunkTokens &&
+           (chunk / 2) % block_size == 0) {
+        chunk /= 2;
+        n_split = (max_ctx + chunk - 1) / chunk;
+    }
+    if (n_split > 65535) return false;
+    plan->chunk = chunk;
+    plan->n_split_max = static_cast<int>(n_split);
     plan->counters_bytes = ((8 + 4 * static_cast<size_t>(num_seqs) * hg + 255) / 256) * 256;
     const size_t rows = static_cast<size_t>(n_split) * num_seqs * Hq;
     plan->lse_offset = plan->counters_bytes;

@@ -33,6 +33,8 @@ int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t
 int encode_f32_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                    const uint32_t* box);
 
+// The current device in *dev_out; ATTN_ERR_UNSUPPORTED unless it is compute capability 10.3.
+int check_device(int* dev_out);
 // Device address of the library's error word on the current device (nullptr on failure).
 unsigned* device_error_word();
 

@@ -241,6 +241,77 @@ def decode_config_inputs(cfg: DecodeConfig, seed=None, poison=False):
                          extra_blocks=cfg.extra_blocks, poison=poison)
 
 
+@dataclass(frozen=True)
+class DecodeStepConfig:
+    """One decode step of an n-layer model: every layer has its own cache and queries; the
+    block table and lengths belong to the sequences and are shared by the layers."""
+    name: str
+    n_layers: int
+    num_seqs: int
+    Hq: int
+    Hkv: int
+    d: int
+    block_size: int
+    len_lo: int
+    len_hi: int
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# A small-batch decode step of a 32-layer model (the pages' launch-overhead example counts
+# a 32-layer decode step; they give no batch or lengths): 8 sequences of 512..2048 tokens.
+C8 = DecodeStepConfig("C8_decode_step_L32_S8_Hq32_Hkv8_d128_bs16_L512_2k", 32, 8, 32, 8, 128, 16, 512, 2048)
+DECODE_STEP_CONFIGS = {C8.name: C8}
+
+
+@dataclass
+class DecodeStepInputs:
+    q: list                    # per layer [S][Hq][d] bf16
+    k_cache: list              # per layer [num_blocks][Hkv][bs][d] bf16
+    v_cache: list
+    block_table: torch.Tensor  # [S][max_blocks] int32, shared by the layers
+    seq_lens: torch.Tensor     # [S] int32, shared by the layers
+    block_size: int
+
+    def layer(self, l: int) -> PagedDecodeInputs:
+        return PagedDecodeInputs(q=self.q[l], k_cache=self.k_cache[l], v_cache=self.v_cache[l],
+                                 block_table=self.block_table, seq_lens=self.seq_lens, block_size=self.block_size)
+
+    @property
+    def kv_bytes(self) -> int:
+        """Bytes of K and V the sequences own, summed over the layers."""
+        return len(self.q) * self.layer(0).kv_bytes
+
+
+def decode_step_inputs(n_layers, num_seqs, Hq, Hkv, d, block_size, seq_lens=None, len_lo=1, len_hi=1, seed=0,
+                       extra_blocks=0, max_blocks_per_seq=None, poison=False):
+    """Layer 0 is ``decode_inputs(..., seed)``; layer l > 0 draws its q and caches from a
+    generator seeded with (seed, l) and shares layer 0's table, lengths and (with
+    ``poison``) NaN pattern in the slots no sequence owns."""
+    base = decode_inputs(num_seqs, Hq, Hkv, d, block_size, seq_lens=seq_lens, len_lo=len_lo, len_hi=len_hi,
+                         seed=seed, extra_blocks=extra_blocks, max_blocks_per_seq=max_blocks_per_seq, poison=poison)
+    qs, ks, vs = [base.q], [base.k_cache], [base.v_cache]
+    unowned = torch.isnan(base.k_cache) if poison else None
+    for l in range(1, n_layers):
+        gen = torch.Generator().manual_seed(int(seed) * 1_000_003 + l)
+        qs.append(_bf16_normal(gen, tuple(base.q.shape)))
+        for lst in (ks, vs):
+            c = _bf16_normal(gen, tuple(base.k_cache.shape))
+            if unowned is not None:
+                c.masked_fill_(unowned, float("nan"))
+            lst.append(c)
+    return DecodeStepInputs(q=qs, k_cache=ks, v_cache=vs, block_table=base.block_table, seq_lens=base.seq_lens,
+                            block_size=block_size)
+
+
+def decode_step_config_inputs(cfg: DecodeStepConfig, seed=None, poison=False):
+    return decode_step_inputs(cfg.n_layers, cfg.num_seqs, cfg.Hq, cfg.Hkv, cfg.d, cfg.block_size, len_lo=cfg.len_lo,
+                              len_hi=cfg.len_hi, seed=cfg.seed if seed is None else seed, poison=poison)
+
+
 @dataclass
 class PagedPrefillInputs:
     q: torch.Tensor            # [S][Hq][max_q][d] bf16

@@ -251,10 +251,56 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         int num_blocks, float scale, void* stream);
 
 /*
- * attn_decode_chunk_tokens -- keys per split-KV chunk attn_decode uses for these sizes
- * (AK FlashDecoding: the chunk length of the split). Informational; 0 if invalid.
+ * attn_decode_graph_create / _launch / _layers / _destroy -- one decode step over many
+ * layers, captured once as a CUDA graph and replayed with a single launch per step.
+ *
+ *   AK, the passage on launch overhead at decode and its remedies (capture the whole
+ *   sequence of launches once and replay it as one unit: the per-launch CPU cost goes,
+ *   the memory traffic stays), applied to the decode of attn_decode.
+ *
+ *   create: n_layers in [1, 4096]. q, k_cache, v_cache, o, lse are HOST arrays of
+ *     n_layers DEVICE pointers, layer l's tensors with the layouts of attn_decode; the
+ *     arrays are read during the call only. block_table, seq_lens, the sizes, scale and
+ *     workspace are those of attn_decode and are shared by every layer (one block table
+ *     per sequence; each layer has its own cache). The layers run in order, one after
+ *     another, so one workspace of attn_decode_workspace_size(...) bytes serves them all.
+ *     Captures, on a private stream, what attn_decode would enqueue for each layer (a
+ *     counter memset and one kernel) and instantiates it; nothing runs. On success
+ *     *graph_out holds an opaque handle (host memory and CUDA graph objects owned by the
+ *     library until attn_decode_graph_destroy); on failure it is NULL. Errors: the
+ *     attn_decode statuses, checked for every layer before any CUDA call; ATTN_ERR_CUDA if
+ *     the capture or the instantiation fails. Call it outside any stream capture of the
+ *     calling thread.
+ *   launch: enqueues the captured step on `stream` (a stream of the device that was
+ *     current at create; another device gives ATTN_ERR_INVALID_ARG). The graph holds
+ *     every pointer and size given at create: keep those buffers alive and in place. It
+ *     reads the CONTENTS at launch time, so between launches the caller may rewrite the
+ *     queries, the cache rows, the block table and seq_lens (the lengths may grow up to
+ *     max_blocks_per_seq * block_size: the split plan depends on sizes only). Two launches
+ *     of one graph, or a launch and another call that share its workspace, must not
+ *     overlap on the device. The device error word works as for attn_decode.
+ *   layers: the layer count of a handle (0 for NULL).
+ *   destroy: releases the handle (NULL is a no-op). Do not destroy a graph whose launch
+ *     may still be running on the device; synchronise the stream first.
  */
-int attn_decode_chunk_tokens(int num_seqs, int Hkv, int block_size, int max_blocks_per_seq);
+int attn_decode_graph_create(int n_layers, const void* const* q, const void* const* k_cache,
+                             const void* const* v_cache, void* const* o, float* const* lse,
+                             const int32_t* block_table, const int32_t* seq_lens, int num_seqs, int Hq,
+                             int Hkv, int d, int block_size, int max_blocks_per_seq, int num_blocks,
+                             float scale, void* workspace, size_t workspace_bytes, void** graph_out);
+int attn_decode_graph_launch(void* graph, void* stream);
+int attn_decode_graph_layers(const void* graph);
+int attn_decode_graph_destroy(void* graph);
+
+/*
+ * attn_decode_chunk_tokens -- keys per split-KV chunk attn_decode uses for these sizes
+ * (AK FlashDecoding: the chunk length of the split). 512 keys, halved (down to 128, and
+ * staying a multiple of block_size) while the work items -- chunks of the longest
+ * possible sequence x num_seqs x kv heads x groups of 16 query heads -- number fewer
+ * than the 1216 worker warps of a full GB300. Depends on sizes only, never on the
+ * lengths. Informational; 0 if invalid.
+ */
+int attn_decode_chunk_tokens(int num_seqs, int Hq, int Hkv, int block_size, int max_blocks_per_seq);
 
 /*
  * attn_get_device_error -- wait for `stream`, then read and clear the device error

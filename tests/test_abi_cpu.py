@@ -170,11 +170,47 @@ def test_decode_argument_validation(lib):
     assert dec(lib, S=0) == 0                 # empty batch: no launch
 
 
+def graph_create(lib, n=2, bad_layer=None, field=None, value=None, S=4, Hq=8, Hkv=2, d=128, bs=16, mb=64, nb=256,
+                 scale=0.1, ws=FAKE, ws_bytes=None, out_ptr=True):
+    """attn_decode_graph_create with fake pointers; (field, value) replaces one pointer of
+    layer ``bad_layer`` (q, kc, vc, o, lse)."""
+    if ws_bytes is None:
+        ws_bytes = lib.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb)
+    arrs = {}
+    for name in ("q", "kc", "vc", "o", "lse"):
+        vals = [FAKE] * max(n, 1)
+        if name == field and bad_layer is not None:
+            vals[bad_layer] = value
+        arrs[name] = (ctypes.c_void_p * len(vals))(*vals)
+    h = ctypes.c_void_p(0x1234)
+    rc = lib.attn_decode_graph_create(n, arrs["q"], arrs["kc"], arrs["vc"], arrs["o"], arrs["lse"], FAKE, FAKE, S, Hq,
+                                      Hkv, d, bs, mb, nb, scale, ws, ws_bytes, ctypes.byref(h) if out_ptr else None)
+    return rc, h.value
+
+
+def test_decode_graph_argument_validation(lib):
+    """Every layer's pointers are checked before any CUDA call; the handle is NULL on failure."""
+    assert graph_create(lib, n=0) == (-1, None)
+    assert graph_create(lib, n=5000) == (-1, None)
+    assert graph_create(lib, out_ptr=False)[0] == -1
+    assert graph_create(lib, n=3, bad_layer=2, field="vc", value=None) == (-1, None)
+    assert graph_create(lib, n=3, bad_layer=1, field="kc", value=FAKE + 4) == (-3, None)
+    assert graph_create(lib, n=3, bad_layer=2, field="lse", value=FAKE + 2) == (-3, None)
+    assert graph_create(lib, d=80) == (-2, None)
+    assert graph_create(lib, bs=24) == (-2, None)
+    assert graph_create(lib, Hq=6, Hkv=4) == (-1, None)
+    assert graph_create(lib, ws_bytes=16) == (-4, None)
+    assert graph_create(lib, ws=FAKE + 8) == (-3, None)
+    assert lib.attn_decode_graph_launch(None, None) == -1
+    assert lib.attn_decode_graph_layers(None) == 0
+    assert lib.attn_decode_graph_destroy(None) == 0
+
+
 def test_workspace_size_matches_split_plan(lib):
     """Counters (8-byte work counter + one int per (sequence, kv head)), then the fp32
     partial log-sums and partial outputs of every possible split, 256-byte aligned."""
     S, Hq, Hkv, d, bs, mb = 64, 32, 8, 128, 16, 2048
-    chunk = eta.attn_decode_chunk_tokens(S, Hkv, bs, mb)
+    chunk = eta.attn_decode_chunk_tokens(S, Hq, Hkv, bs, mb)
     n_split = -(-mb * bs // chunk)
     rows = n_split * S * Hq
     up = lambda x: -(-x // 256) * 256
@@ -184,11 +220,34 @@ def test_workspace_size_matches_split_plan(lib):
     assert chunk % bs == 0 and chunk % 16 == 0
 
 
+def test_split_plan_halves_chunk_for_small_batches(lib):
+    """Fewer items than worker warps (1216): the chunk halves, down to 128 keys, staying a
+    multiple of the block size; large batches keep 512."""
+    def items(S, Hq, Hkv, bs, mb):
+        chunk = eta.attn_decode_chunk_tokens(S, Hq, Hkv, bs, mb)
+        return chunk, -(-mb * bs // chunk) * S * Hkv * -(-(Hq // Hkv) // 16)
+    assert items(64, 32, 8, 16, 2048)[0] == 512           # the long decode workload
+    chunk, n = items(8, 32, 8, 16, 125)                    # 8 sequences of <= 2000 tokens
+    assert chunk == 128 and n == 16 * 8 * 8                # the floor: 1024 items
+    chunk, n = items(8, 32, 8, 16, 250)                    # <= 4000 tokens
+    assert chunk == 128 and n == 32 * 8 * 8                # 256 would give 16 x 64 = 1024 items
+    assert items(1, 8, 1, 16, 4)[0] == 128                 # tiny: floor of 128 keys
+    assert items(1, 8, 1, 128, 4)[0] == 128                # stays a multiple of a 128-token block
+    assert items(1, 8, 1, 256, 4)[0] == 256
+    assert items(2, 64, 2, 16, 64)[0] == 128               # 32 query heads per kv head: 2 groups
+    assert items(80, 64, 2, 16, 64)[0] == 256              # 80 seqs x 2 kv x 2 groups x 4 splits = 1280
+    # the workspace follows the plan
+    S, Hq, Hkv, d, bs, mb = 8, 32, 8, 128, 16, 125
+    rows = (mb * bs // 128 + (mb * bs % 128 > 0)) * S * Hq
+    up = lambda x: -(-x // 256) * 256
+    assert eta.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb) == up(8 + 4 * S * Hkv) + up(rows * 4) + rows * d * 4
+
+
 def test_split_plan_reproduces_flashdecoding_example(lib):
     with open(os.path.join(GOLDEN, "flashdecoding_split_example.json")) as f:
         g = json.load(f)
     mb = g["kv_len"] // g["block_size"]
-    chunk = eta.attn_decode_chunk_tokens(g["batch"], g["heads"], g["block_size"], mb)
+    chunk = eta.attn_decode_chunk_tokens(g["batch"], g["heads"], g["heads"], g["block_size"], mb)
     assert chunk == g["chunk"]
     n_split = g["kv_len"] // chunk
     assert n_split == g["chunks"]
