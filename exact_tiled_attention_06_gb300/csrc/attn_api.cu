@@ -287,7 +287,7 @@ ATTN_API int attn_decode(const void* q, const void* k_cache, const void* v_cache
     if (!err) return kErrCuda;
     return launch_decode(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, d, block_size,
                          max_blocks_per_seq, num_blocks, scale, workspace, plan, static_cast<cudaStream_t>(stream),
-                         err);
+                         err, 0);
 }
 
 ATTN_API int attn_get_device_error(void* stream)

@@ -2,10 +2,11 @@
 //
 // One persistent kernel, one block per SM, eight independent worker warps per block.
 // A work item is (key chunk of 512 tokens -- fewer for a small batch, down to 128 -- kv
-// head [, group of 16 query heads], sequence). Each warp repeatedly:
-//   * takes the next item from a device-wide counter (items in split-major order;
-//     chunks that lie past their sequence's end are skipped on the device, so the
-//     host never reads the sequence lengths),
+// head [, group of 16 query heads], sequence). Each block first reads the sequence
+// lengths (on the device: the host never reads them) and prefix-sums their chunk counts
+// in shared memory, so items exist only inside sequences. Each warp then repeatedly:
+//   * takes an item: its own index first, then the next one from a device-wide counter
+//     (items in sequence order -- most chunks first -- then head group, then chunk),
 //   * loads the item's block-table entries (one per lane) and the query heads of its
 //     kv head as mma.sync A fragments,
 //   * streams the chunk's 16-token K and V sub-pages with TMA (128-byte swizzle) into
@@ -16,6 +17,11 @@
 //   * writes the chunk's normalised partial and log-sum; the warp that completes the
 //     last chunk of a (sequence, head group) merges all its partials and writes O and
 //     lse. A sequence that fits in one chunk is written directly.
+// Every launch leaves its counters at zero (the merging warp resets its completion
+// counter, the last warp to leave resets the claim counters), and every block signals
+// programmatic dependents at its start and waits for its own predecessor before touching
+// outputs or workspace, so a chain of decode launches (the layers of a captured step)
+// needs one memset and overlaps each launch's set-up with the previous one's tail.
 //
 // Pages: "Modern attention kernels", "Prefill and decode need different kernels"
 // (decode is memory-bound: wide contiguous cache reads, one query's context spread over
@@ -45,6 +51,8 @@ constexpr int kMinChunkTokens = 128;  // keys per work item (the fewest the plan
 constexpr long long kTargetItems = 152 * 8;  // worker warps of a full GB300 (152 SMs x 8)
 constexpr int kMaxChunkBlocks = 32;   // block-table entries per item (one per lane)
 constexpr int kRowsPerItem = 16;      // query heads per item (mma M)
+constexpr int kPlanMaxSeqs = 2048;    // sequences per launch (the block's length table)
+static_assert(kPlanMaxSeqs <= 2048, "the sort key holds the sequence in 11 bits");
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -59,8 +67,11 @@ struct DecCfg {
     static constexpr int kWarpRingBytes = kStages * kStageBytes;
     static constexpr int kBarOff = kDecWarps * kWarpRingBytes;
     static constexpr int kUsedBytes = kBarOff + kDecWarps * kStages * 8;
-    static constexpr int kSmemBytes = kUsedBytes + 1024;
-    static_assert(kUsedBytes <= 227 * 1024, "shared memory budget");
+    // lengths, chunk prefix, per-warp scan totals, sequences in heaviest-first order
+    static constexpr int kPlanOff = kUsedBytes;
+    static constexpr int kPlanBytes = (3 * kPlanMaxSeqs + 2 + kDecWarps) * 4;
+    static constexpr int kSmemBytes = kPlanOff + kPlanBytes + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct DecParams {
@@ -69,11 +80,11 @@ struct DecParams {
     const int32_t* seq_lens;
     __nv_bfloat16* o;
     float* lse;
-    unsigned long long* work;  // next work item
+    unsigned long long* work;  // dynamic items claimed after each warp's first
+    unsigned* exits;           // blocks that have left the work loop
     int* done;                 // [num_seqs][HG] chunks finished
     float* part_o;             // [n_split_max][num_seqs][Hq][D]
     float* part_lse;           // [n_split_max][num_seqs][Hq], log2 units
-    long long n_slots;         // n_split_max * num_seqs * HG
     int num_seqs, Hq, Hkv, G, block_size, max_blocks, num_blocks;
     int chunk;
     int n_hgroups;
@@ -113,13 +124,81 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     const uint32_t bar0 = smem_u32(smem) + C::kBarOff + warp * C::kStages * 8;
     auto full = [&](int s) { return bar0 + 8u * s; };
 
+    if (threadIdx.x == 0) griddep_launch_dependents();  // the next launch may start its set-up
     if (lane == 0) {
         for (int s = 0; s < C::kStages; ++s) mbar_init(full(s), 1);
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
-    __syncwarp();
+    // ---- the block's plan: every sequence's length and its number of chunks (an empty
+    // sequence has one item, which writes O = 0 and lse = -inf); the sequences sorted by
+    // chunk count, most first (the longest work is taken first, so the last items of the
+    // launch are short ones); the chunk counts prefix-summed in that order, so that item t
+    // maps to (sequence, chunk, head group) with no item past a sequence's end.
+    int* sL = reinterpret_cast<int*>(smem + C::kPlanOff);  // [num_seqs] lengths
+    int* sP = sL + kPlanMaxSeqs;                            // [num_seqs + 1] prefix, sorted order
+    int* warp_tot = sP + kPlanMaxSeqs + 1;                  // [kDecWarps]
+    volatile int* sDry = warp_tot + kDecWarps;              // a warp of this block found no item left
+    int* sKey = warp_tot + kDecWarps + 1;                   // [pow2 >= num_seqs] sort keys
+    {
+        constexpr int kThreads = kDecWarps * 32;
+        const int S = p.num_seqs;
+        int N = 1;
+        while (N < S) N <<= 1;
+        // key = (65535 - chunks) << 11 | sequence: ascending keys = most chunks first, ties
+        // in sequence order (chunks <= 65535 and sequence < 2048 per launch)
+        for (int i = threadIdx.x; i < N; i += kThreads) {
+            int key = INT_MAX;
+            if (i < S) {
+                const int L = clamp_len(p, p.seq_lens[i]);
+                sL[i] = L;
+                const int n = L > 0 ? (L + p.chunk - 1) / p.chunk : 1;
+                key = ((65535 - n) << 11) | i;
+            }
+            sKey[i] = key;
+        }
+        __syncthreads();
+        for (int k = 2; k <= N; k <<= 1) {  // bitonic sort in shared memory
+            for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                for (int i = threadIdx.x; i < N; i += kThreads) {
+                    const int ixj = i ^ jj;
+                    if (ixj > i) {
+                        const int a = sKey[i], b = sKey[ixj];
+                        if ((a > b) == ((i & k) == 0)) {
+                            sKey[i] = b;
+                            sKey[ixj] = a;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        // exclusive prefix of the chunk counts in sorted order (contiguous runs per thread)
+        const int per = (S + kThreads - 1) / kThreads;
+        const int b0 = threadIdx.x * per;
+        const int b1 = min(S, b0 + per);
+        int mine = 0;
+        for (int i = b0; i < b1; ++i) mine += 65535 - (sKey[i] >> 11);
+        int incl = mine;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += warp_tot[w];
+        int run = base + incl - mine;
+        for (int i = b0; i < b1; ++i) {
+            sP[i] = run;
+            run += 65535 - (sKey[i] >> 11);
+        }
+        if (threadIdx.x == kThreads - 1) sP[S] = base + incl;
+        if (threadIdx.x == 0) *sDry = 0;
+        __syncthreads();
+    }
 
     const int g = lane >> 2;   // fragment row group
     const int tig = lane & 3;  // thread in group
@@ -130,26 +209,57 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     const int v_token = 8 * (mat & 1) + rr, v_unit = mat >> 1;
     uint32_t uses = 0;  // sub-pages this warp has streamed (ring position)
 
+    // Items in heaviest-first sequence order, then head group, then chunk: a sequence's
+    // chunks are taken together, so its merge can start early. Each warp's first item is its own index
+    // (nothing to claim); later ones come from a device-wide counter.
+    const int n_warps = static_cast<int>(gridDim.x) * kDecWarps;
+    const long long n_items = static_cast<long long>(sP[p.num_seqs]) * p.HG;
+    bool first = true;
+    bool waited = false;
+    // Work written by the previous launch (outputs, this launch's workspace) is touched
+    // only after it has completed; set-up and cache reads may overlap its tail.
+    auto wait_prior = [&]() {
+        if (!waited) {
+            griddep_wait();
+            waited = true;
+        }
+    };
     while (true) {
         // ---------------------------------------------------------------- next item
-        long long slot = 0;
-        int L = 0;
-        if (lane == 0) {
-            while (true) {
-                slot = static_cast<long long>(atomicAdd(p.work, 1ull));
-                if (slot >= p.n_slots) break;
-                const int split = static_cast<int>(slot / (static_cast<long long>(p.num_seqs) * p.HG));
-                const int seq = static_cast<int>((slot / p.HG) % p.num_seqs);
-                L = clamp_len(p, p.seq_lens[seq]);
-                if (split == 0 || static_cast<long long>(split) * p.chunk < L) break;
-            }
+        long long t = 0;
+        if (first) {
+            t = static_cast<long long>(blockIdx.x) * kDecWarps + warp;
+            first = false;
+        } else {
+            // nothing to claim when the first items covered everything, or once another
+            // warp of this block has found the counter exhausted
+            int dry = 0;
+            if (lane == 0) dry = *sDry;
+            dry = __shfl_sync(0xffffffffu, dry, 0);  // one decision for the whole warp
+            if (n_items <= n_warps || dry) break;
+            wait_prior();
+            if (lane == 0) t = n_warps + static_cast<long long>(atomicAdd(p.work, 1ull));
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t >= n_items && lane == 0) *sDry = 1;
         }
-        slot = __shfl_sync(0xffffffffu, slot, 0);
-        L = __shfl_sync(0xffffffffu, L, 0);
-        if (slot >= p.n_slots) break;
-        const int split = static_cast<int>(slot / (static_cast<long long>(p.num_seqs) * p.HG));
-        const int seq = static_cast<int>((slot / p.HG) % p.num_seqs);
-        const int hg = static_cast<int>(slot % p.HG);
+        if (t >= n_items) break;
+        const int qi = static_cast<int>(t / p.HG);  // in chunk units: sP[pos] <= qi < sP[pos + 1]
+        int pos = 0;                                 // place in the heaviest-first order
+        {
+            int lo = 0, hi = p.num_seqs - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sP[mid] <= qi) lo = mid;
+                else hi = mid - 1;
+            }
+            pos = lo;
+        }
+        const int seq = sKey[pos] & 2047;
+        const int n_chunks = sP[pos + 1] - sP[pos];
+        const int rem = static_cast<int>(t - static_cast<long long>(sP[pos]) * p.HG);
+        const int hg = rem / n_chunks;
+        const int split = rem % n_chunks;
+        const int L = sL[seq];
         const int hkv = hg / p.n_hgroups;
         const int grp = hg % p.n_hgroups;
         const int hq0 = hkv * p.G + grp * kRowsPerItem;
@@ -158,6 +268,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
 
         if (L == 0) {
             // an empty sequence: O = 0, lse = -inf
+            wait_prior();
             for (int idx = lane; idx < nvalid * D; idx += 32)
                 p.o[out_row0 * D + idx] = __float2bfloat16_rn(0.0f);
             if (lane < nvalid) p.lse[out_row0 + lane] = -INFINITY;
@@ -196,6 +307,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         const int primed = min(C::kStages, n_sub);
         for (int i = 0; i < primed; ++i) issue(i);
         int issued = primed;
+        wait_prior();
 
         // q as A fragments (rows = query heads of this kv head, zero past nvalid)
         uint32_t qa[D / 16][4];
@@ -311,7 +423,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
             }
         }
         uses += static_cast<uint32_t>(issued);
-        if (!ok) return;
+        if (!ok) break;  // a copy timed out (reported): leave through the exit count
 
         // ---------------------------------------------------------------- item result
 #pragma unroll
@@ -434,6 +546,20 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 }
             }
         }
+        if (lane == 0) p.done[static_cast<size_t>(seq) * p.HG + hg] = 0;  // the last to touch it
+    }
+    // ---- leave: the last block of the grid puts the claim counters back to zero, so the
+    // next launch on this workspace needs no memset (the completion counters were reset
+    // by the warps that merged). Every warp of the block has stopped claiming here.
+    wait_prior();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.exits, 1u) == gridDim.x - 1) {
+            *p.work = 0ull;
+            *p.exits = 0u;
+            __threadfence();
+        }
     }
 }
 
@@ -457,12 +583,14 @@ template <int D>
 int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                     const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int block_size,
                     int max_blocks, int num_blocks, float scale, void* workspace, const DecodePlan& plan,
-                    cudaStream_t stream, unsigned* err)
+                    cudaStream_t stream, unsigned* err, int flags)
 {
     using C = DecCfg<D>;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    // the work counter and the completion counters must start at zero
-    if (cudaMemsetAsync(ws, 0, plan.counters_bytes, stream) != cudaSuccess) return kErrCuda;
+    // the claim counters and the completion counters must start at zero; every launch
+    // leaves them at zero again, so a chain of launches needs this only once
+    if (!(flags & kDecodeCountersZeroed) && cudaMemsetAsync(ws, 0, plan.counters_bytes, stream) != cudaSuccess)
+        return kErrCuda;
     CUtensorMap tk, tv;
     const uint64_t dims[2] = {static_cast<uint64_t>(D),
                               static_cast<uint64_t>(num_blocks) * Hkv * static_cast<uint64_t>(block_size)};
@@ -472,17 +600,17 @@ int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, con
     if (rc != kOk) return rc;
     rc = encode_bf16_map(&tv, v_cache, 2, dims, strides, box);
     if (rc != kOk) return rc;
+    const int sms = sm_count();
+    if (sms <= 0) return kErrCuda;
+    if (cudaFuncSetAttribute(attn_decode_sm103<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return kErrCuda;
     DecParams prm;
-    prm.q = static_cast<const __nv_bfloat16*>(q);
-    prm.block_table = block_table;
-    prm.seq_lens = seq_lens;
-    prm.o = static_cast<__nv_bfloat16*>(o);
-    prm.lse = lse;
     prm.work = reinterpret_cast<unsigned long long*>(ws);
-    prm.done = reinterpret_cast<int*>(ws + 8);
+    prm.exits = reinterpret_cast<unsigned*>(ws + 8);
+    prm.done = reinterpret_cast<int*>(ws + 16);
     prm.part_lse = reinterpret_cast<float*>(ws + plan.lse_offset);
     prm.part_o = reinterpret_cast<float*>(ws + plan.o_offset);
-    prm.num_seqs = num_seqs;
     prm.Hq = Hq;
     prm.Hkv = Hkv;
     prm.G = Hq / Hkv;
@@ -492,17 +620,36 @@ int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, con
     prm.chunk = plan.chunk;
     prm.n_hgroups = plan.n_hgroups;
     prm.HG = Hkv * plan.n_hgroups;
-    prm.n_slots = static_cast<long long>(plan.n_split_max > 0 ? plan.n_split_max : 1) * num_seqs * prm.HG;
     prm.scale_log2 = scale * kLog2e;
     prm.err = err;
-    const int sms = sm_count();
-    if (sms <= 0) return kErrCuda;
-    long long grid = sms;
-    if (grid * kDecWarps > prm.n_slots) grid = (prm.n_slots + kDecWarps - 1) / kDecWarps;
-    if (cudaFuncSetAttribute(attn_decode_sm103<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
-        return kErrCuda;
-    attn_decode_sm103<D><<<static_cast<unsigned>(grid), kDecWarps * 32, C::kSmemBytes, stream>>>(tk, tv, prm);
+    // A block holds the lengths of at most kPlanMaxSeqs sequences: larger batches run as
+    // consecutive launches over ranges of sequences (the later ones chained to the earlier).
+    for (int s0 = 0; s0 < num_seqs; s0 += kPlanMaxSeqs) {
+        const int S = num_seqs - s0 < kPlanMaxSeqs ? num_seqs - s0 : kPlanMaxSeqs;
+        prm.q = static_cast<const __nv_bfloat16*>(q) + static_cast<size_t>(s0) * Hq * D;
+        prm.block_table = block_table + static_cast<size_t>(s0) * max_blocks;
+        prm.seq_lens = seq_lens + s0;
+        prm.o = static_cast<__nv_bfloat16*>(o) + static_cast<size_t>(s0) * Hq * D;
+        prm.lse = lse + static_cast<size_t>(s0) * Hq;
+        prm.num_seqs = S;
+        // at most one item per warp beyond what the batch can hold
+        const long long max_items =
+            static_cast<long long>(plan.n_split_max > 0 ? plan.n_split_max : 1) * S * prm.HG;
+        long long grid = sms;
+        if (grid * kDecWarps > max_items) grid = (max_items + kDecWarps - 1) / kDecWarps;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kDecWarps * 32);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        const bool chained = (flags & kDecodeChained) || s0 > 0;
+        cfg.attrs = chained ? attr : nullptr;
+        cfg.numAttrs = chained ? 1 : 0;
+        if (cudaLaunchKernelEx(&cfg, attn_decode_sm103<D>, tk, tv, prm) != cudaSuccess) return kErrLaunch;
+    }
     return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 
@@ -533,7 +680,7 @@ bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_b
     if (n_split > 65535) return false;
     plan->chunk = chunk;
     plan->n_split_max = static_cast<int>(n_split);
-    plan->counters_bytes = ((8 + 4 * static_cast<size_t>(num_seqs) * hg + 255) / 256) * 256;
+    plan->counters_bytes = ((16 + 4 * static_cast<size_t>(num_seqs) * hg + 255) / 256) * 256;
     const size_t rows = static_cast<size_t>(n_split) * num_seqs * Hq;
     plan->lse_offset = plan->counters_bytes;
     plan->o_offset = plan->lse_offset + ((rows * 4 + 255) / 256) * 256;
@@ -544,14 +691,14 @@ bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_b
 int launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                   const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
                   int max_blocks_per_seq, int num_blocks, float scale, void* workspace, const DecodePlan& plan,
-                  cudaStream_t stream, unsigned* err)
+                  cudaStream_t stream, unsigned* err, int flags)
 {
     if (d == 128)
         return launch_decode_d<128>(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, block_size,
-                                    max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err);
+                                    max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err, flags);
     if (d == 64)
         return launch_decode_d<64>(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, block_size,
-                                   max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err);
+                                   max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err, flags);
     return kErrUnsupported;
 }
 
@@ -637,5 +784,5 @@ extern "C" __attribute__((visibility("default"))) int attn_decode_noalloc(
     if (!err) return kErrCuda;
     return launch_decode(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, d, block_size,
                          max_blocks_per_seq, num_blocks, scale, scratch, plan, static_cast<cudaStream_t>(stream),
-                         err);
+                         err, 0);
 }

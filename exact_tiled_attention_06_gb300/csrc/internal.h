@@ -61,7 +61,8 @@ struct DecodePlan {
     int chunk;              // keys per split (multiple of 16 and of block_size)
     int n_split_max;        // splits of the longest possible sequence
     int n_hgroups;          // groups of at most 16 query heads per kv head
-    size_t counters_bytes;  // work counter (8 bytes) + one completion counter per (sequence, head group)
+    size_t counters_bytes;  // claim counter (8 bytes), exit counter (4 + 4 pad), one completion counter
+                            // per (sequence, head group)
     size_t lse_offset;      // byte offset of the partial log-sums  [n_split_max][num_seqs][Hq] fp32
     size_t o_offset;        // byte offset of the partial outputs   [n_split_max][num_seqs][Hq][d] fp32
     size_t bytes;           // total workspace bytes
@@ -69,11 +70,18 @@ struct DecodePlan {
 bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
                  DecodePlan* plan);
 
-// Decode (implemented in decode_kernel.cu). Arguments are already validated.
+// Decode (implemented in decode_kernel.cu). Arguments are already validated. flags:
+//   kDecodeCountersZeroed -- the workspace's counters are known to be zero (the previous
+//                            launch on it completed normally): no memset is enqueued;
+//   kDecodeChained        -- launch as a programmatic dependent of the previous launch on
+//                            the stream (its set-up and cache reads overlap that launch's
+//                            tail; everything else waits for it to complete).
+constexpr int kDecodeCountersZeroed = 1;
+constexpr int kDecodeChained = 2;
 int launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                   const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
                   int block_size, int max_blocks_per_seq, int num_blocks, float scale, void* workspace,
-                  const DecodePlan& plan, cudaStream_t stream, unsigned* err);
+                  const DecodePlan& plan, cudaStream_t stream, unsigned* err, int flags);
 
 // Backward workspace: D_i [B][Hq][Nq] fp32 at dvec_offset, then the fp32 dQ accumulator
 // [B][Hq][Nq][d] at dq_offset (256-byte aligned).

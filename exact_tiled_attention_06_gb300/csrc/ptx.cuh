@@ -29,6 +29,21 @@ __device__ __forceinline__ void report_error(unsigned* err, unsigned code)
     if (err) atomicCAS(err, 0u, code);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Let the launch that follows this one on the stream (when it was launched as a
+// programmatic dependent) begin once every block of this grid has issued this or exited.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grid this launch depends on has completed and its memory operations are
+// visible; returns at once for a launch without such a dependency.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {

@@ -216,8 +216,8 @@ size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int bloc
  *   Cache slots past a sequence's length (the tail of its last block) are never used,
  *   whatever they hold. A block-table entry outside [0, num_blocks) sets
  *   ATTN_ERR_DEVICE_BOUNDS in the device error word (the output is then undefined).
- *   Enqueues a 4-byte-granular memset of the workspace's counters and one kernel on
- *   `stream`. Returns ATTN_OK or a negative attn_status.
+ *   Enqueues a 4-byte-granular memset of the workspace's counters and one kernel per
+ *   2048 sequences on `stream`. Returns ATTN_OK or a negative attn_status.
  */
 int attn_decode(const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,
@@ -264,8 +264,11 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
  *     workspace are those of attn_decode and are shared by every layer (one block table
  *     per sequence; each layer has its own cache). The layers run in order, one after
  *     another, so one workspace of attn_decode_workspace_size(...) bytes serves them all.
- *     Captures, on a private stream, what attn_decode would enqueue for each layer (a
- *     counter memset and one kernel) and instantiates it; nothing runs. On success
+ *     Captures, on a private stream, one counter memset and then each layer's decode
+ *     kernel(s); every decode launch leaves the counters at zero, so layers after the
+ *     first need no memset and are launched as programmatic dependents of the layer
+ *     before (their set-up and first cache reads overlap its tail; everything they write
+ *     waits for it to complete). Then instantiates the graph; nothing runs. On success
  *     *graph_out holds an opaque handle (host memory and CUDA graph objects owned by the
  *     library until attn_decode_graph_destroy); on failure it is NULL. Errors: the
  *     attn_decode statuses, checked for every layer before any CUDA call; ATTN_ERR_CUDA if
@@ -276,7 +279,9 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
  *     every pointer and size given at create: keep those buffers alive and in place. It
  *     reads the CONTENTS at launch time, so between launches the caller may rewrite the
  *     queries, the cache rows, the block table and seq_lens (the lengths may grow up to
- *     max_blocks_per_seq * block_size: the split plan depends on sizes only). Two launches
+ *     max_blocks_per_seq * block_size: the split plan depends on sizes only). A layer's
+ *     caches must not overlap an earlier layer's o or lse (a dependent layer starts
+ *     reading its caches before its predecessor ends; it reads q only after). Two launches
  *     of one graph, or a launch and another call that share its workspace, must not
  *     overlap on the device. The device error word works as for attn_decode.
  *   layers: the layer count of a handle (0 for NULL).

@@ -140,3 +140,35 @@ def test_full_c5_sampled_sequences(oracle):
     o_ref, lse_ref = oracle_decode(oracle, x, c.scale, seqs)
     check_attention(o.cpu()[seqs], lse.cpu()[seqs], o_ref, lse_ref, "C5 sampled")
     assert torch.all(torch.isfinite(o))
+
+
+def test_more_sequences_than_one_launch_holds(oracle):
+    """2500 sequences run as two launches (2048 + 452): sequences on both sides of the cut
+    against the oracle, with empty and one-token sequences among them."""
+    gen = torch.Generator().manual_seed(21)
+    lens = torch.randint(0, 41, (2500,), generator=gen).tolist()
+    lens[2047], lens[2048], lens[2499] = 0, 1, 40
+    x = inputs.decode_inputs(2500, 8, 2, 64, 16, seq_lens=lens, seed=21, extra_blocks=4, poison=True)
+    o, lse = run_decode(x, 0.125)
+    seqs = [0, 1, 2, 1000, 2046, 2047, 2048, 2049, 2300, 2499]
+    o_ref, lse_ref = oracle_decode(oracle, x, 0.125, seqs=seqs)
+    check_attention(o[seqs], lse[seqs], o_ref, lse_ref, "2500 sequences")
+
+
+def test_counters_left_at_zero_for_the_next_call():
+    """Every launch puts its counters back to zero: a workspace reused by back-to-back calls
+    of different batches gives the same results as fresh workspaces."""
+    xa = inputs.decode_inputs(6, 8, 2, 128, 16, len_lo=1, len_hi=3000, seed=22)
+    xb = inputs.decode_inputs(3, 8, 2, 128, 16, len_lo=1, len_hi=700, seed=23, max_blocks_per_seq=190)
+    ws = torch.zeros(max(eta.attn_decode_workspace_size(6, 8, 2, 128, 16, xa.block_table.shape[1]),
+                         eta.attn_decode_workspace_size(3, 8, 2, 128, 16, xb.block_table.shape[1])),
+                     dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(128)
+    ref_a, ref_b = run_decode(xa, scale), run_decode(xb, scale)
+    for _ in range(3):
+        for x, ref in ((xa, ref_a), (xb, ref_b)):
+            o, lse = run_decode(x, scale, workspace=ws)
+            assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1])
+    n_ctr = 16 + 4 * 6 * 2  # claim counter, exit counter and pad, one completion counter per (seq, kv head)
+    torch.cuda.synchronize()
+    assert int(ws[:n_ctr].count_nonzero()) == 0

@@ -159,3 +159,37 @@ def test_full_c8_step_sampled(oracle):
         o_ref, lse_ref = oracle_decode(oracle, x.layer(l), scale, seqs=seqs)
         check_attention(g.out[l][seqs], g.lse[l][seqs], o_ref, lse_ref, f"C8 layer {l}")
     g.close()
+
+
+def test_graph_and_per_call_decode_share_a_workspace():
+    x = inputs.decode_step_inputs(3, 4, 8, 2, 128, 16, len_lo=1, len_hi=2500, seed=16)
+    qs, ks, vs, bt, sl = to_cuda(x)
+    scale = 1.0 / math.sqrt(128)
+    ws = torch.empty(eta.attn_decode_workspace_size(4, 8, 2, 128, 16, bt.shape[1]), dtype=torch.uint8, device="cuda")
+    ref = eager(qs, ks, vs, bt, sl, scale)
+    g = eta.attn_decode_graph_create(qs, ks, vs, bt, sl, scale=scale, workspace=ws)
+    for _ in range(2):
+        g.launch()
+        o1, lse1 = eta.attn_decode(qs[1], ks[1], vs[1], bt, sl, scale=scale, workspace=ws)
+        torch.cuda.synchronize()
+        for l in range(3):
+            assert torch.equal(g.out[l], ref[l][0]) and torch.equal(g.lse[l], ref[l][1])
+        assert torch.equal(o1, ref[1][0])
+    g.close()
+
+
+def test_graph_over_more_sequences_than_one_launch_holds(oracle):
+    """2100 sequences: each layer is two chained launches inside the graph."""
+    gen = torch.Generator().manual_seed(17)
+    lens = torch.randint(0, 70, (2100,), generator=gen).tolist()
+    x = inputs.decode_step_inputs(2, 2100, 8, 2, 64, 16, seq_lens=lens, seed=17, extra_blocks=2, poison=True)
+    qs, ks, vs, bt, sl = to_cuda(x)
+    g = eta.attn_decode_graph_create(qs, ks, vs, bt, sl, scale=0.125)
+    g.launch()
+    torch.cuda.synchronize()
+    assert eta.attn_get_device_error() == 0
+    seqs = [0, 5, 2047, 2048, 2099]
+    for l in range(2):
+        o_ref, lse_ref = oracle_decode(oracle, x.layer(l), 0.125, seqs=seqs)
+        check_attention(g.out[l][seqs], g.lse[l][seqs], o_ref, lse_ref, f"2100 sequences layer {l}")
+    g.close()
