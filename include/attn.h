@@ -254,9 +254,10 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
  * attn_decode_graph_create / _launch / _layers / _destroy -- one decode step over many
  * layers, captured once as a CUDA graph and replayed with a single launch per step.
  *
- *   AK, the passage on launch overhead at decode and its remedies (capture the whole
- *   sequence of launches once and replay it as one unit: the per-launch CPU cost goes,
- *   the memory traffic stays), applied to the decode of attn_decode.
+ *   AK, the passage on launch overhead at decode and its remedies (a decode step repeats
+ *   identical launches, so they are recorded a single time and re-issued together: the
+ *   host pays per step instead of per launch, while the bytes moved do not change),
+ *   applied to the decode of attn_decode.
  *
  *   create: n_layers in [1, 4096]. q, k_cache, v_cache, o, lse are HOST arrays of
  *     n_layers DEVICE pointers, layer l's tensors with the layouts of attn_decode; the
