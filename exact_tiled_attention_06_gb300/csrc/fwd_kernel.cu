@@ -247,6 +247,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // ---- dense and sparse: the Q tiles (and, dense, the first K/V tiles) are requested as
+    // soon as the barriers exist, ahead of the TMEM allocation and (sparse) the walk: their
+    // latency is the longest part of a short block's start. Sparse: both tiles' Q is loaded
+    // even if the walk later finds a tile with no listed block. Paged: the producer loads Q
+    // (measured: issuing it here does not help there).
+    auto issue_q = [&]() {
+        uint32_t qbytes = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            if (act[t]) qbytes += C::kTileBytes;
+        mbar_arrive_expect_tx(bar_q, qbytes);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (!act[t]) continue;
+#pragma unroll
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_3d(sb + C::kQOff + t * C::kTileBytes + x * C::kBoxBytes, &tm_q, bar_q, 64 * x, tw[t].row0,
+                            b * p.Hq + tw[t].head);
+        }
+    };
+    const bool q_early = has_work && !PAGED;
+    const int n_pre = (MODE == kModeDense && has_work) ? min(C::kStages, 2 * (hi - lo)) : 0;  // even
+    if (threadIdx.x == 0 && q_early) {
+        fence_proxy_async_smem();
+        issue_q();
+        for (int i = 0; i < n_pre; ++i) {  // first fill of each ring slot: K_lo, V_lo, K_lo+1, ...
+            mbar_arrive_expect_tx(kv_full(i), C::kTileBytes);
+            const CUtensorMap* map = (i & 1) == 0 ? &tm_k : &tm_v;
+#pragma unroll
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_3d(sb + C::kRingOff + i * C::kTileBytes + x * C::kBoxBytes, map, kv_full(i), 64 * x,
+                            (lo + i / 2) * BN, b * p.Hkv + hkv);
+        }
+    }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
         tmem_relinquish();
@@ -342,26 +376,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     if (warp == kLoadWarp) {
         // ================================================================ producer
-        if (has_work && lane == 0) {
-            uint32_t qbytes = 0;
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                if (act[t]) qbytes += C::kTileBytes;
-            mbar_arrive_expect_tx(bar_q, qbytes);
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (!act[t]) continue;
-#pragma unroll
-                for (int x = 0; x < C::kBoxes; ++x)
-                    tma_load_3d(sQ + t * C::kTileBytes + x * C::kBoxBytes, &tm_q, bar_q, 64 * x, tw[t].row0,
-                                b * p.Hq + tw[t].head);
-            }
-        }
-        int n = 0;  // K/V copies issued (K and V alternate in the ring)
+        if (PAGED && has_work && lane == 0) issue_q();
+        int n = n_pre;  // K/V copies issued (K and V alternate in the ring)
         if constexpr (!PAGED) {
             if (has_work && lane == 0) {
                 bool ok = true;
-                for (int e = 0; e < n_walk && ok; ++e) {
+                for (int e = n_pre / 2; e < n_walk && ok; ++e) {
                     const int j = walk_j(e);
 #pragma unroll
                     for (int kind = 0; kind < 2; ++kind) {
@@ -458,7 +478,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
         }
-        if (has_work && lane == 0) {
+        if ((has_work || q_early) && lane == 0) {
             // Never leave while a copy into this block's shared memory is in flight.
             mbar_wait(bar_q, 0, nullptr, p.err);
             for (int s = 0; s < C::kStages; ++s) {
