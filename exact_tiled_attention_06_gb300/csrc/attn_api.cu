@@ -52,6 +52,24 @@ int check_device(int* dev_out)
     return g_arch_ok[dev] == 1 ? kOk : kErrUnsupported;
 }
 
+namespace {
+int g_num_sms[kMaxDevices] = {};
+std::mutex g_sm_mu;
+}  // namespace
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_sm_mu);
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_num_sms[dev] = n;
+    }
+    return g_num_sms[dev];
+}
+
 unsigned* device_error_word()
 {
     int dev = 0;

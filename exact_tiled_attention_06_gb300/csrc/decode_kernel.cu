@@ -563,21 +563,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     }
 }
 
-int g_num_sms[64] = {};
-std::mutex g_sm_mu;
-
-int sm_count()
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    std::lock_guard<std::mutex> lk(g_sm_mu);
-    if (g_num_sms[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        g_num_sms[dev] = n;
-    }
-    return g_num_sms[dev];
-}
 
 template <int D>
 int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,

@@ -94,6 +94,7 @@ struct FwdParams {
     int pair_heads;    // 1: tiles are query heads (2u, 2u+1) at one row tile; 0: row tiles (2r, 2r+1)
     int n_row_units;   // row units per (batch, head unit)
     int n_hunits;      // head units per batch entry
+    int next_stride;   // dense / sparse: units between a block and the one that will take its SM
     unsigned* err;
 };
 
@@ -398,6 +399,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             tma_load_3d(sRing + s * C::kTileBytes + x * C::kBoxBytes, map, kv_full(s), 64 * x, j * BN,
                                         b * p.Hkv + hkv);
                         ++n;
+                    }
+                }
+                // The block that will run on this SM after this one is about next_stride
+                // units further on: bring its Q tiles and first K/V tile into L2 now, so that
+                // its start does not wait on DRAM.
+                const long long un = static_cast<long long>(blockIdx.x) + p.next_stride;
+                if (p.next_stride > 0 && un < gridDim.x) {
+                    const int u2 = static_cast<int>(un);
+                    const int n_bh = p.B * p.n_hunits;
+                    const int ru2 = p.n_row_units - 1 - u2 / n_bh;
+                    const int bh2 = u2 % n_bh;
+                    const int b2 = bh2 / p.n_hunits, hu2 = bh2 % p.n_hunits;
+                    TileWork t2[2];
+                    if (p.pair_heads) {
+                        t2[0] = make_tile(p, 2 * hu2, ru2 * BM, p.Nq, p.Nk);
+                        t2[1] = make_tile(p, 2 * hu2 + 1, ru2 * BM, p.Nq, p.Nk);
+                    } else {
+                        t2[0] = make_tile(p, hu2, 2 * ru2 * BM, p.Nq, p.Nk);
+                        t2[1] = make_tile(p, hu2, (2 * ru2 + 1) * BM, p.Nq, p.Nk);
+                    }
+                    int lo2 = INT_MAX;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (t2[t].rows <= 0) continue;
+#pragma unroll
+                        for (int x = 0; x < C::kBoxes; ++x)
+                            tma_prefetch_l2_3d(&tm_q, 64 * x, t2[t].row0, b2 * p.Hq + t2[t].head);
+                        if (t2[t].kv_lo < t2[t].kv_hi) lo2 = min(lo2, t2[t].kv_lo);
+                    }
+                    if (!SPARSE && lo2 != INT_MAX && p.Nk > 0) {
+                        const int hkv2 = t2[0].head / p.G;
+#pragma unroll
+                        for (int x = 0; x < C::kBoxes; ++x) {
+                            tma_prefetch_l2_3d(&tm_k, 64 * x, lo2 * BN, b2 * p.Hkv + hkv2);
+                            tma_prefetch_l2_3d(&tm_v, 64 * x, lo2 * BN, b2 * p.Hkv + hkv2);
+                        }
                     }
                 }
             }
@@ -800,6 +837,7 @@ int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* ls
     prm.max_blocks = prm.block_size = prm.bs_log2 = prm.num_blocks = 0;
     prm.row_ptr = row_ptr;
     prm.col_idx = col_idx;
+    prm.next_stride = sm_count();  // one block per SM: the block launched next is about this far on
     prm.err = err;
     const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
@@ -872,6 +910,7 @@ int launch_fwd_paged_d(const void* q, const void* k_cache, const void* v_cache, 
     const int n_row_tiles = (max_q + BM - 1) / BM;
     prm.n_row_units = prm.pair_heads ? n_row_tiles : (n_row_tiles + 1) / 2;
     prm.n_hunits = prm.pair_heads ? Hq / 2 : Hq;
+    prm.next_stride = 0;
     prm.err = err;
     const long long grid = static_cast<long long>(S) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;

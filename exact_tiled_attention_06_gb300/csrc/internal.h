@@ -35,6 +35,8 @@ int encode_f32_map(CUtensorMap* map, const void* base, int rank, const uint64_t*
 
 // The current device in *dev_out; ATTN_ERR_UNSUPPORTED unless it is compute capability 10.3.
 int check_device(int* dev_out);
+// Number of SMs of the current device (0 on failure), looked up once per device.
+int sm_count();
 // Device address of the library's error word on the current device (nullptr on failure).
 unsigned* device_error_word();
 
