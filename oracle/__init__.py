@@ -87,6 +87,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                                                              c_int]
     lib.oracle_attn_prefill_paged.argtypes = [_D, _D, _D, _I32, _I32, _I32, _D, _D] + [c_int] * 8 + [c_double, c_int,
                                                                                                    c_int]
+    _U8 = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = c_double
+    lib.oracle_e4m3_decode.argtypes = [_U8, _D, ctypes.c_int64]
+    lib.oracle_attn_fwd_fp8.argtypes = [_U8, _U8, _U8, _D, _D] + [c_int] * 6 + [c_double] * 4 + [c_int, c_int]
     lib.oracle_num_threads.argtypes = []
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows, lib.oracle_attn_fwd_blocked,
               lib.oracle_attn_fwd_split, lib.oracle_attn_decode, lib.oracle_attn_bwd, lib.oracle_attn_prefill_paged,
@@ -114,6 +119,10 @@ def _f64(a) -> np.ndarray:
 
 def _p(a: np.ndarray):
     return a.ctypes.data_as(_D)
+
+
+def _pu8(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
 
 
 def _check(rc: int, name: str) -> None:
@@ -183,6 +192,30 @@ class Oracle:
         _check(self.lib.oracle_attn_fwd_split(_p(q), _p(k), _p(v), _p(o), _p(lse), B, Hq, Hkv, Nq, Nk, d,
                                               float(scale), int(bool(causal)), int(window), int(chunk)),
                "oracle_attn_fwd_split")
+        return o, lse
+
+    def e4m3_decode(self, codes):
+        """Real values of 8-bit E4M3 codes (uint8 array, any shape)."""
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.zeros(c.shape, dtype=np.float64)
+        _check(self.lib.oracle_e4m3_decode(_pu8(c), _p(out), c.size), "oracle_e4m3_decode")
+        return out
+
+    def attn_fwd_fp8(self, q8, k8, vt8, scale, q_descale, k_descale, v_descale, causal=False, window=-1):
+        """Attention over E4M3 codes: q8 [B][Hq][Nq][d], k8 [B][Hkv][Nk][d], vt8 [B][Hkv][d][Nk]
+        (uint8), real values = code value x the tensor's descale. Returns (o, lse) in fp64."""
+        q8 = np.ascontiguousarray(q8, dtype=np.uint8)
+        k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+        vt8 = np.ascontiguousarray(vt8, dtype=np.uint8)
+        B, Hq, Nq, d = q8.shape
+        Bk, Hkv, Nk, dk = k8.shape
+        if Bk != B or dk != d or vt8.shape != (B, Hkv, d, Nk):
+            raise ValueError("fp8 shapes disagree")
+        o = np.zeros((B, Hq, Nq, d))
+        lse = np.zeros((B, Hq, Nq))
+        _check(self.lib.oracle_attn_fwd_fp8(_pu8(q8), _pu8(k8), _pu8(vt8), _p(o), _p(lse), B, Hq,
+                                            Hkv, Nq, Nk, d, float(scale), float(q_descale), float(k_descale),
+                                            float(v_descale), int(bool(causal)), int(window)), "oracle_attn_fwd_fp8")
         return o, lse
 
     def attn_bwd(self, q, k, v, dout, scale, causal=False, window=-1):
@@ -294,6 +327,14 @@ def attn_prefill_paged(*a, **kw):
 
 def attn_fwd_blocksparse(*a, **kw):
     return default().attn_fwd_blocksparse(*a, **kw)
+
+
+def e4m3_decode(*a, **kw):
+    return default().e4m3_decode(*a, **kw)
+
+
+def attn_fwd_fp8(*a, **kw):
+    return default().attn_fwd_fp8(*a, **kw)
 
 
 def num_threads() -> int:

@@ -19,6 +19,7 @@
  *
  * Layouts (row-major, contiguous):
  *   q, o : [B][Hq][Nq][d]      k, v : [B][Hkv][Nk][d]      lse : [B][Hq][Nq]
+ *   FP8 variant: 8-bit E4M3 codes, V transposed (see oracle_attn_fwd_fp8)
  *   paged caches : [num_blocks][Hkv][block_size][d]
  *   block_table  : int32 [num_seqs][max_blocks_per_seq]
  *
@@ -668,6 +669,67 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
         free(dp);
     }
     return err;
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8 (E4M3) inputs.                                                          */
+/* [AK] the FlashAttention-3 paragraph lists FP8 operands among the Hopper-era  */
+/*   additions; the attention computed is still the plain definition above,    */
+/*   applied to the real values that the 8-bit codes and per-tensor scales      */
+/*   denote.                                                                    */
+/* The E4M3 code (the OCP 8-bit floating-point format, E4M3 variant): bit 7 is  */
+/*   the sign, bits 6..3 the exponent with bias 7, bits 2..0 the mantissa.      */
+/*   Exponent field 0 is subnormal: value = mantissa / 8 * 2^-6. Exponent 15    */
+/*   with mantissa 7 is NaN; there is no infinity (exponent 15 with mantissa    */
+/*   0..6 is an ordinary number, up to 448).                                    */
+/* Layouts: q8 [B][Hq][Nq][d], k8 [B][Hkv][Nk][d], vt8 [B][Hkv][d][Nk] (V given */
+/*   transposed: element (j, t) of head h's V is vt8[h][t][j]).                 */
+/* ------------------------------------------------------------------------- */
+double oracle_e4m3_value(uint8_t code)
+{
+    const int negative = (code >> 7) & 1;
+    const int exponent = (code >> 3) & 15;
+    const int mantissa = code & 7;
+    double magnitude;
+    if (exponent == 15 && mantissa == 7) return NAN;
+    if (exponent == 0)
+        magnitude = ldexp((double)mantissa / 8.0, -6);
+    else
+        magnitude = ldexp(1.0 + (double)mantissa / 8.0, exponent - 7);
+    return negative ? -magnitude : magnitude;
+}
+
+int oracle_e4m3_decode(const uint8_t* codes, double* out, int64_t n)
+{
+    if (n < 0) return ORACLE_EINVAL;
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]);
+    return ORACLE_OK;
+}
+
+int oracle_attn_fwd_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* vt8, double* o, double* lse,
+                        int B, int Hq, int Hkv, int Nq, int Nk, int d, double scale,
+                        double q_descale, double k_descale, double v_descale, int causal, int window)
+{
+    if (check_dims(B, Hq, Hkv, Nq, Nk, d)) return ORACLE_EINVAL;
+    const int64_t nq = (int64_t)B * Hq * Nq * d;
+    const int64_t nk = (int64_t)B * Hkv * Nk * d;
+    double* q = (double*)malloc(sizeof(double) * (size_t)(nq > 0 ? nq : 1));
+    double* k = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    double* v = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    if (!q || !k || !v) {
+        free(q); free(k); free(v);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t i = 0; i < nq; ++i) q[i] = q_descale * oracle_e4m3_value(q8[i]);
+    for (int64_t i = 0; i < nk; ++i) k[i] = k_descale * oracle_e4m3_value(k8[i]);
+    /* v[b][h][j][t] = v_descale * value(vt8[b][h][t][j]) */
+    for (int64_t bh = 0; bh < (int64_t)B * Hkv; ++bh)
+        for (int64_t j = 0; j < Nk; ++j)
+            for (int t = 0; t < d; ++t)
+                v[(bh * Nk + j) * d + t] = v_descale * oracle_e4m3_value(vt8[(bh * d + t) * Nk + j]);
+    const int rc = oracle_attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, window);
+    free(q); free(k); free(v);
+    return rc;
 }
 
 /* Number of OpenMP threads the oracle will use (reported beside CPU timings). */

@@ -514,6 +514,85 @@ def pin_blocksparse_block_diagonal_is_segments(orc):
         _close(lse[:, :, sl], ls_, 1e-14, f"segment {t} lse")
 
 
+def pin_e4m3_decode(orc):
+    """E4M3 codes: closed forms from the format definition, strict order of the positive
+    codes, and all 256 codes against torch's float8_e4m3fn conversion."""
+    closed = {0x38: 1.0, 0x7E: 448.0, 0x01: 2.0 ** -9, 0x07: 7.0 / 8 * 2.0 ** -6, 0x08: 2.0 ** -6, 0xB8: -1.0,
+              0x40: 2.0, 0x30: 0.5, 0x3C: 1.5, 0x77: 240.0, 0x00: 0.0}
+    codes = np.array(list(closed), dtype=np.uint8)
+    _close(orc.e4m3_decode(codes), np.array(list(closed.values())), 0.0, "e4m3 closed forms")
+    z = orc.e4m3_decode(np.array([0x80, 0x7F, 0xFF], dtype=np.uint8))
+    assert z[0] == 0.0 and np.signbit(z[0]) and np.isnan(z[1]) and np.isnan(z[2]), "e4m3 -0 / NaN codes"
+    pos = orc.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0), "positive E4M3 codes must increase strictly"
+    try:
+        import torch
+    except ImportError:
+        return
+    allc = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(allc.copy()).view(torch.float8_e4m3fn).float().double().numpy()
+    got = orc.e4m3_decode(allc)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "e4m3 NaN codes differ from torch"
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]), "e4m3 values differ from torch float8_e4m3fn"
+
+
+def _fp8_case(seed, B, Hq, Hkv, Nq, Nk, d):
+    r = _rng(seed)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    q8 = r.choice(finite, (B, Hq, Nq, d))
+    k8 = r.choice(finite, (B, Hkv, Nk, d))
+    vt8 = r.choice(finite, (B, Hkv, d, Nk))
+    return q8, k8, vt8
+
+
+def pin_fp8_numpy_bruteforce(orc):
+    """FP8 attention = numpy softmax attention over the decoded values (decoded by torch's
+    float8_e4m3fn, V transposed back with numpy) times the per-tensor scales."""
+    try:
+        import torch
+    except ImportError:
+        return
+    dec = lambda c: torch.from_numpy(np.ascontiguousarray(c)).view(torch.float8_e4m3fn).double().numpy()
+    for mi, (Nq, Nk, causal, window) in enumerate(MASKS[:5]):
+        q8, k8, vt8 = _fp8_case(2100 + mi, 1, 2, 1, Nq, Nk, 4)
+        qs, ks, vs, sc = 0.003, 0.0021, 0.013, 0.5
+        o, lse = orc.attn_fwd_fp8(q8, k8, vt8, sc, qs, ks, vs, causal, window)
+        q = dec(q8) * qs
+        k = np.repeat(dec(k8) * ks, 2, axis=1)
+        v = np.repeat(np.swapaxes(dec(vt8), 2, 3) * vs, 2, axis=1)
+        i = np.arange(Nq)[:, None]
+        j = np.arange(Nk)[None, :]
+        diag = i + (Nk - Nq)
+        keep = np.ones((Nq, Nk), dtype=bool)
+        if causal:
+            keep &= j <= diag
+        if window >= 0:
+            keep &= j >= diag - window
+        s_ = sc * np.einsum("bhid,bhjd->bhij", q, k)
+        s_ = np.where(keep, s_, -np.inf)
+        m = s_.max(axis=-1, keepdims=True)
+        e = np.where(keep, np.exp(s_ - np.where(np.isfinite(m), m, 0.0)), 0.0)
+        l = e.sum(axis=-1, keepdims=True)
+        pr = np.divide(e, l, out=np.zeros_like(e), where=l > 0)
+        _close(o, np.einsum("bhij,bhjd->bhid", pr, v), 1e-13, f"fp8 numpy O {mi}")
+        ref_lse = np.where(l[..., 0] > 0, m[..., 0] + np.log(np.where(l[..., 0] > 0, l[..., 0], 1.0)), -np.inf)
+        _close(lse, ref_lse, 1e-12, f"fp8 numpy lse {mi}")
+
+
+def pin_fp8_scale_folding(orc):
+    """The scales enter as the definition says: doubling q's scale equals doubling the
+    softmax scale; V's scale multiplies O and leaves lse unchanged."""
+    q8, k8, vt8 = _fp8_case(2200, 1, 2, 2, 9, 11, 8)
+    o1, l1 = orc.attn_fwd_fp8(q8, k8, vt8, 0.3, 0.02, 0.01, 0.05, True, -1)
+    o2, l2 = orc.attn_fwd_fp8(q8, k8, vt8, 0.6, 0.01, 0.01, 0.05, True, -1)
+    _close(o1, o2, 1e-14, "fp8 q scale vs softmax scale (O)")
+    _close(l1, l2, 1e-12, "fp8 q scale vs softmax scale (lse)")
+    o3, l3 = orc.attn_fwd_fp8(q8, k8, vt8, 0.3, 0.02, 0.01, 0.1, True, -1)
+    _close(o3, 2.0 * o1, 1e-14, "fp8 v scale multiplies O")
+    _close(l3, l1, 0.0, "fp8 v scale leaves lse")
+
+
 ALL_PINS = [
     pin_blocked_equals_materialised,
     pin_split_equals_unsplit,
@@ -538,4 +617,7 @@ ALL_PINS = [
     pin_blocksparse_full_pattern_is_dense,
     pin_blocksparse_numpy_bruteforce,
     pin_blocksparse_block_diagonal_is_segments,
+    pin_e4m3_decode,
+    pin_fp8_numpy_bruteforce,
+    pin_fp8_scale_folding,
 ]

@@ -40,6 +40,11 @@ MUTANTS = [
     ("blocksparse_dense_mask_ignored", "if (key_allowed(i, j, Nq, Nk, causal, window) &&\n                            block_listed",
      "if (j < Nk &&\n                            block_listed"),
     ("blocksparse_key_block_by_query_size", "i / block_q, j / block_k))", "i / block_q, j / block_q))"),
+    ("e4m3_exponent_bias_8", "(double)mantissa / 8.0, exponent - 7)", "(double)mantissa / 8.0, exponent - 8)"),
+    ("e4m3_subnormal_scale", "ldexp((double)mantissa / 8.0, -6);", "ldexp((double)mantissa / 8.0, -7);"),
+    ("e4m3_no_nan_code", "if (exponent == 15 && mantissa == 7) return NAN;", ""),
+    ("fp8_v_not_transposed", "vt8[(bh * d + t) * Nk + j]", "vt8[(bh * Nk + j) * d + t]"),
+    ("fp8_missing_k_scale", "k[i] = k_descale * oracle_e4m3_value(k8[i]);", "k[i] = oracle_e4m3_value(k8[i]);"),
 ]
 
 
