@@ -15,6 +15,9 @@ attn_prefill_paged on the chunked-prefill workload (16 sequences, 2048 new queri
 each over a paged cache) the same way; ``--no-paged-prefill`` skips it. ``blocksparse``
 times attn_fwd_blocksparse on a 32k-token global + local block pattern the same way
 (4 * d FLOPs per allowed pair of the listed blocks); ``--no-blocksparse`` skips it.
+``fp8_prefill`` times attn_fwd_fp8 on the long causal workload quantised per tensor to
+E4M3 (same FLOP count; roofline against twice the measured bf16 peak);
+``--no-fp8`` skips it.
 ``decode_graph`` times a 32-layer decode step (8 sequences, each layer its own cache) two
 ways: one attn_decode call per layer, and the same calls captured once with
 attn_decode_graph_create and replayed with one graph launch per step (KV GB/s over the
@@ -152,6 +155,7 @@ KERNEL_SOURCES = {
     "attn_bwd_sm103": ("bwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_fwd_sm103_paged": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_fwd_sm103_sparse": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_fwd_sm103_fp8": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
 }
 
 
@@ -462,6 +466,23 @@ def run_ours(args, rank, world, local_rank):
 
         bs_ms = timed_loop(run_bs, "block-sparse prefill")
 
+    # ---- FP8 prefill: the long causal workload quantised per tensor to E4M3, in a loop of
+    #      its own (inputs 128 MiB + O 64 MiB, above L2)
+    f8_ms = None
+    if args.workload in ("both", "prefill") and not args.no_fp8:
+        fx = inputs.fp8_prefill_inputs(pc.B, pc.Hq, pc.Hkv, pc.Nq, pc.Nk, pc.d, seed=pc.seed + rank,
+                                       k_boost_frac=pc.k_boost_frac)
+        fq, fk, fvt = fx.q8.to(dev), fx.k8.to(dev), fx.vt8.to(dev)
+        fo = torch.empty(fq.shape, dtype=torch.bfloat16, device=dev)
+        flse = torch.empty(fq.shape[:3], dtype=torch.float32, device=dev)
+        f8_flops = attention_flops(pc.B, pc.Hq, pc.Nq, pc.Nk, pc.d, pc.causal, pc.window)
+
+        def run_f8():
+            eta.attn_fwd_fp8(fq, fk, fvt, fx.q_descale, fx.k_descale, fx.v_descale, causal=pc.causal,
+                             window=pc.window, scale=pc.scale, out=fo, lse=flse)
+
+        f8_ms = timed_loop(run_f8, "FP8 prefill")
+
     # ---- a many-layer decode step (every layer its own cache): one attn_decode call per
     #      layer from the host, against the same calls captured once as a CUDA graph and
     #      replayed with one launch per step (the step's KV, ~1 GB, exceeds L2)
@@ -495,7 +516,9 @@ def run_ours(args, rank, world, local_rank):
     extra = ([float(bwd_ms.mean())] if bwd_ms is not None else []) + ([float(pp_ms.mean())] if pp_ms is not None else [])
     extra += [float(bs_ms.mean())] if bs_ms is not None else []
     extra += [float(eager_ms.mean()), float(graph_ms.mean())] if graph_ms is not None else []
+    extra += [float(f8_ms.mean())] if f8_ms is not None else []
     vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms + extra, world, dev)
+    f8_mean = vals.pop() if f8_ms is not None else None
     graph_mean = vals.pop() if graph_ms is not None else None
     eager_mean = vals.pop() if graph_ms is not None else None
     bs_mean = vals.pop() if bs_ms is not None else None
@@ -622,6 +645,23 @@ def run_ours(args, rank, world, local_rank):
                          "ms_per_launch": round(bs_mean, 4),
                          "ms_p10_p50_p90": [round(float(np.percentile(bs_ms, x)), 4) for x in (10, 50, 90)]},
         }
+    if f8_ms is not None:
+        achieved = f8_flops / (f8_mean * 1e-3) / 1e12
+        fp8_peak = 2.0 * peaks["bf16_tflops"]  # measured bf16 dense x the nominal fp8 : bf16 ratio (2)
+        result["fp8_prefill"] = {
+            "value": round(whole_job_rate(f8_flops, world, f8_mean, 1e12), 2), "unit": "TFLOP/s",
+            "workload": pc.name + "_e4m3", "flops_per_launch": f8_flops, "steps": args.steps, "warmup": args.warmup,
+            "gpu_launches": args.steps, "dtype": "e4m3 Q/K/V, fp32 accumulation, bf16 O",
+            "config": {"B": pc.B, "Hq": pc.Hq, "Hkv": pc.Hkv, "N": pc.Nq, "d": pc.d, "causal": pc.causal,
+                       "scales": "per tensor, max|x| / 448"},
+            "roofline": {"kernel": "attn_fwd_sm103<128, fp8>", "bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                         "peak_kind": f"{peak_kind} bf16 dense burst x 2 (nominal fp8 : bf16)",
+                         "frac_of_bf16_peak": round(achieved / peaks["bf16_tflops"], 4),
+                         "traffic": load_traffic("attn_fwd_sm103_fp8"),
+                         "ms_per_launch": round(f8_mean, 4),
+                         "ms_p10_p50_p90": [round(float(np.percentile(f8_ms, x)), 4) for x in (10, 50, 90)]},
+        }
     if graph_ms is not None:
         achieved = g_kv / (graph_mean * 1e-3) / 1e9
         result["decode_graph"] = {
@@ -734,6 +774,7 @@ def main():
     ap.add_argument("--no-decode-graph", action="store_true",
                     help="skip the many-layer decode step (per-call launches against one CUDA-graph replay)")
     ap.add_argument("--no-blocksparse", action="store_true", help="skip the block-sparse prefill measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (E4M3) prefill measurement")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences than the workload's 64")
     args = ap.parse_args()

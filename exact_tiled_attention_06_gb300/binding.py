@@ -24,7 +24,7 @@ STATUS_NAMES = {
 }
 
 # Every symbol include/attn.h declares.
-EXPORTED = ("attn_fwd", "attn_fwd_blocksparse", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
+EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
             "attn_decode_noalloc", "attn_decode_graph_create", "attn_decode_graph_launch", "attn_decode_graph_layers",
             "attn_decode_graph_destroy")
@@ -57,6 +57,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         lib.attn_fwd.restype = i
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, i, i, vp]
+        lib.attn_fwd_fp8.restype = i
         lib.attn_fwd_blocksparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, vp]
         lib.attn_fwd_blocksparse.restype = i
         lib.attn_prefill_paged.argtypes = [vp] * 8 + [i] * 8 + [f, i, i, vp]
@@ -149,6 +151,42 @@ def attn_fwd(q, k, v, causal=False, window=-1, scale=None, out=None, lse=None, s
                                  float(scale), int(bool(causal)), int(window), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def _need_u8(t, name: str, ndim: int):
+    """An E4M3 tensor: uint8 or torch.float8_e4m3fn, CUDA, contiguous; returned as uint8."""
+    if isinstance(t, torch.Tensor) and t.dtype == getattr(torch, "float8_e4m3fn", None):
+        t = t.view(torch.uint8)
+    _need(t, name, torch.uint8, ndim)
+    return t
+
+
+def attn_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, causal=False, window=-1, scale=None, out=None,
+                 lse=None, stream=None):
+    """FP8 prefill. q8 [B][Hq][Nq][128], k8 [B][Hkv][Nk][128], vt8 [B][Hkv][128][Nk] E4M3 (uint8 or
+    float8_e4m3fn, CUDA); real inputs = codes x the per-tensor descales. ``scale`` defaults to
+    1/sqrt(d). Returns (o bf16 [B][Hq][Nq][128], lse fp32 [B][Hq][Nq])."""
+    q8 = _need_u8(q8, "q8", 4)
+    k8 = _need_u8(k8, "k8", 4)
+    vt8 = _need_u8(vt8, "vt8", 4)
+    B, Hq, Nq, d = q8.shape
+    Bk, Hkv, Nk, dk = k8.shape
+    if Bk != B or dk != d or tuple(vt8.shape) != (B, Hkv, d, Nk):
+        raise ValueError("q8/k8/vt8 shapes disagree")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q8.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    rc = load_library().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                     float(scale), float(q_descale), float(k_descale), float(v_descale),
+                                     int(bool(causal)), int(window), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
     return out, lse
 
 

@@ -126,6 +126,13 @@ int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t
                       strides_bytes, box);
 }
 
+int encode_u8_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                  const uint32_t* box)
+{
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_128B, base, rank, dims, strides_bytes,
+                      box);
+}
+
 int encode_f32_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                    const uint32_t* box)
 {
@@ -143,7 +150,7 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       int Nq, int Nk, int d, float scale, int causal, int window, void* stream)
 {
     // ---- arguments (no CUDA call before these checks)
-    if (!q || !o || !lse) return kErrInvalidArg;
+    if ((!q || !o || !lse) && Nq != 0) return kErrInvalidArg;  // no queries: nothing is read or written
     if ((!k || !v) && Nk != 0) return kErrInvalidArg;  // no keys: k and v are never read
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return kErrInvalidArg;
     if (Hq % Hkv != 0) return kErrInvalidArg;
@@ -161,6 +168,35 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
     if (!err) return kErrCuda;
     return launch_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, window,
                       static_cast<cudaStream_t>(stream), err);
+}
+
+ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nq, int Nk, int d, float scale, float q_descale, float k_descale, float v_descale,
+                          int causal, int window, void* stream)
+{
+    // ---- arguments (no CUDA call before these checks)
+    if ((!q || !o || !lse) && Nq != 0) return kErrInvalidArg;  // no queries: nothing is read or written
+    if ((!k || !vt) && Nk != 0) return kErrInvalidArg;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0) return kErrInvalidArg;
+    if (Hq % Hkv != 0) return kErrInvalidArg;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return kErrInvalidArg;
+    if (!(q_descale > 0.0f) || !std::isfinite(q_descale) || !(k_descale > 0.0f) || !std::isfinite(k_descale) ||
+        !(v_descale > 0.0f) || !std::isfinite(v_descale))
+        return kErrInvalidArg;
+    if (static_cast<long long>(B) * Hq > INT32_MAX / 2 || static_cast<long long>(B) * Hkv > INT32_MAX / 2)
+        return kErrInvalidArg;
+    if (d != 128) return kErrUnsupported;
+    if (Nk % 16 != 0) return kErrUnsupported;  // the V^T rows (Nk bytes) must stay 16-byte aligned
+    if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned4(lse)) return kErrMisaligned;
+    if (Nq == 0) return kOk;
+    // ---- device
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc != kOk) return rc;
+    unsigned* err = device_error_word();
+    if (!err) return kErrCuda;
+    return launch_fwd_fp8(q, k, vt, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, q_descale, k_descale, v_descale, causal,
+                          window, static_cast<cudaStream_t>(stream), err);
 }
 
 ATTN_API int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

@@ -53,18 +53,25 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kFwdThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: move the max only if it rises by > 256x
+// FP8: the max moves once it rises by > 4x, and p is computed as 2^6 * 2^(s - m), so
+// p <= 2^8 stays inside E4M3's range (448) while probabilities down to 2^-12 of the row's
+// weight keep E4M3's normal (relative) precision. l carries the same 2^6.
+constexpr float kFp8RescaleThreshold = 2.0f;
+constexpr float kFp8PShift = 6.0f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kModeDense = 0, kModePaged = 1, kModeSparse = 2;
+constexpr int kModeFp8 = 3;  // dense over E4M3 Q, K and transposed V (d = 128)
 constexpr int kMaxWalk = 4096;                        // sparse: entries of the merged walk
 constexpr int kWalkBytes = kMaxWalk * 4 + 16;         // entries + {count, last entry of tile 0 / 1}
 
-template <int D>
+template <int D, int EB = 2>  // EB: bytes per Q/K/V element (2: bf16, 1: E4M3)
 struct FwdCfg {
-    static constexpr int kBoxes = D / 64;            // 128-byte-wide TMA boxes per row
+    static constexpr int kBoxCols = 128 / EB;        // elements per 128-byte box row
+    static constexpr int kBoxes = D * EB / 128;      // 128-byte-wide TMA boxes per row
     static constexpr int kBoxBytes = 128 * 128;      // 128 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;
-    static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots (K and V alternate)
+    static constexpr int kStages = (kTileBytes == 2 * kBoxBytes) ? 4 : 8;  // K/V ring slots (K and V alternate)
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
@@ -95,6 +102,7 @@ struct FwdParams {
     int n_row_units;   // row units per (batch, head unit)
     int n_hunits;      // head units per batch entry
     int next_stride;   // dense / sparse: units between a block and the one that will take its SM
+    float out_scale;   // multiplies O (FP8: V's scale; else 1)
     unsigned* err;
 };
 
@@ -154,7 +162,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
 {
-    using C = FwdCfg<D>;
+    constexpr bool FP8 = MODE == kModeFp8;
+    using C = FwdCfg<D, FP8 ? 1 : 2>;
     constexpr bool PAGED = MODE == kModePaged;
     constexpr bool SPARSE = MODE == kModeSparse;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -264,22 +273,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!act[t]) continue;
 #pragma unroll
             for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_3d(sb + C::kQOff + t * C::kTileBytes + x * C::kBoxBytes, &tm_q, bar_q, 64 * x, tw[t].row0,
-                            b * p.Hq + tw[t].head);
+                tma_load_3d(sb + C::kQOff + t * C::kTileBytes + x * C::kBoxBytes, &tm_q, bar_q, C::kBoxCols * x,
+                            tw[t].row0, b * p.Hq + tw[t].head);
+        }
+    };
+    // One K (kind 0) or V (kind 1) tile of key tile j into ring slot s. FP8 V is stored
+    // transposed ([d][Nk] per head): its tile is the 128 keys of every d row, one box.
+    auto load_kv = [&](int kind, int s, int j) {
+        const uint32_t dst = sb + C::kRingOff + s * C::kTileBytes;
+        if (FP8 && kind == 1) {
+            tma_load_3d(dst, &tm_v, kv_full(s), j * BN, 0, b * p.Hkv + hkv);
+        } else {
+            const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+#pragma unroll
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_3d(dst + x * C::kBoxBytes, map, kv_full(s), C::kBoxCols * x, j * BN, b * p.Hkv + hkv);
         }
     };
     const bool q_early = has_work && !PAGED;
-    const int n_pre = (MODE == kModeDense && has_work) ? min(C::kStages, 2 * (hi - lo)) : 0;  // even
+    const int n_pre = ((MODE == kModeDense || FP8) && has_work) ? min(C::kStages, 2 * (hi - lo)) : 0;  // even
     if (threadIdx.x == 0 && q_early) {
         fence_proxy_async_smem();
         issue_q();
         for (int i = 0; i < n_pre; ++i) {  // first fill of each ring slot: K_lo, V_lo, K_lo+1, ...
             mbar_arrive_expect_tx(kv_full(i), C::kTileBytes);
-            const CUtensorMap* map = (i & 1) == 0 ? &tm_k : &tm_v;
-#pragma unroll
-            for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_3d(sb + C::kRingOff + i * C::kTileBytes + x * C::kBoxBytes, map, kv_full(i), 64 * x,
-                            (lo + i / 2) * BN, b * p.Hkv + hkv);
+            load_kv(i & 1, i, lo + i / 2);
         }
     }
     if (warp == kMmaWarp) {
@@ -393,11 +411,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(kv_full(s), C::kTileBytes);
-                        const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
-#pragma unroll
-                        for (int x = 0; x < C::kBoxes; ++x)
-                            tma_load_3d(sRing + s * C::kTileBytes + x * C::kBoxBytes, map, kv_full(s), 64 * x, j * BN,
-                                        b * p.Hkv + hkv);
+                        load_kv(kind, s, j);
                         ++n;
                     }
                 }
@@ -425,15 +439,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         if (t2[t].rows <= 0) continue;
 #pragma unroll
                         for (int x = 0; x < C::kBoxes; ++x)
-                            tma_prefetch_l2_3d(&tm_q, 64 * x, t2[t].row0, b2 * p.Hq + t2[t].head);
+                            tma_prefetch_l2_3d(&tm_q, C::kBoxCols * x, t2[t].row0, b2 * p.Hq + t2[t].head);
                         if (t2[t].kv_lo < t2[t].kv_hi) lo2 = min(lo2, t2[t].kv_lo);
                     }
                     if (!SPARSE && lo2 != INT_MAX && p.Nk > 0) {
                         const int hkv2 = t2[0].head / p.G;
 #pragma unroll
                         for (int x = 0; x < C::kBoxes; ++x) {
-                            tma_prefetch_l2_3d(&tm_k, 64 * x, lo2 * BN, b2 * p.Hkv + hkv2);
-                            tma_prefetch_l2_3d(&tm_v, 64 * x, lo2 * BN, b2 * p.Hkv + hkv2);
+                            tma_prefetch_l2_3d(&tm_k, C::kBoxCols * x, lo2 * BN, b2 * p.Hkv + hkv2);
+                            if (FP8) tma_prefetch_l2_3d(&tm_v, lo2 * BN, 0, b2 * p.Hkv + hkv2);
+                            else tma_prefetch_l2_3d(&tm_v, C::kBoxCols * x, lo2 * BN, b2 * p.Hkv + hkv2);
                         }
                     }
                 }
@@ -526,23 +541,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     } else if (warp == kMmaWarp) {
         // ================================================================ MMA issue
         if (lane == 0 && has_work) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, false, true);
+            constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3_f32(BM, D) : idesc_bf16_f32(BM, D, false, true);
             // S_t = Q_t K^T: both operands K-major; a 16-wide k step is 32 bytes inside a
             // 128-byte swizzle row, and every 64 columns start a new box.
             // Descriptors are built once; another k step, slot or tile only adds its byte
             // offset / 16 to the start-address field (every address stays below 256 KB).
             const uint64_t qdesc0 = smem_desc_sw128(sQ, 16, 1024);
             const uint64_t kdesc0 = smem_desc_sw128(sRing, 16, 1024);
-            const uint64_t vdesc0 = smem_desc_sw128(sRing, C::kBoxBytes, 1024);
+            // bf16 V is MN-major (d contiguous); FP8 V arrives transposed, K-major like K.
+            const uint64_t vdesc0 = FP8 ? smem_desc_sw128(sRing, 16, 1024) : smem_desc_sw128(sRing, C::kBoxBytes, 1024);
             auto issue_qk = [&](int t, int slot) {
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * BN);
                 const uint64_t qd = qdesc0 + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
                 const uint64_t kd = kdesc0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
+                if constexpr (FP8) {
+                    // 32 E4M3 elements (32 bytes) per step, all inside the one 128-byte row
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-                    mma_ss(d_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 32; ++kk)
+                        mma_ss_f8(d_tmem, qd + 2 * kk, kd + 2 * kk, idesc_qk, kk > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
+                        mma_ss(d_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
                 }
             };
             // O_t (+)= P_t V: P from TMEM (8 columns = 16 bf16 keys per step); V is
@@ -552,10 +575,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const uint32_t d_tmem = tmem + C::kOCol + static_cast<uint32_t>(t * D);
                 const uint32_t a_tmem = tmem + static_cast<uint32_t>(t * BN);
                 const uint64_t vd = vdesc0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
+                if constexpr (FP8) {
+                    // P as E4M3 in TMEM: 32 keys = 8 columns per step; V^T K-major: +32 bytes
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), idesc_pv,
-                           (accumulate || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BN / 32; ++kk)
+                        mma_ts_f8(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(2 * kk), idesc_pv,
+                                  (accumulate || kk > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ts(d_tmem, a_tmem + kk * 8, vd + static_cast<uint64_t>(kk * 128), idesc_pv,
+                               (accumulate || kk > 0) ? 1u : 0u);
+                }
             };
 
             bool ok = mbar_wait(bar_q, 0, abort_flag, p.err);
@@ -687,7 +718,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
                 }
                 const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-                const bool need = m_cand > m + kRescaleThreshold || (m == -INFINITY && m_cand > -INFINITY);
+                const bool need = m_cand > m + (FP8 ? kFp8RescaleThreshold : kRescaleThreshold) ||
+                                   (m == -INFINITY && m_cand > -INFINITY);
                 float alpha = 1.0f;
                 const bool rescale = __any_sync(0xffffffffu, need);
                 if (rescale) {
@@ -695,26 +727,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     alpha = (m == -INFINITY) ? 0.0f : ex2_approx(m - m_new);
                     m = m_new;
                 }
-                const float base = (m == -INFINITY) ? 0.0f : m;
+                const float base = (m == -INFINITY) ? 0.0f : (FP8 ? m - kFp8PShift : m);
                 float sum0 = 0.0f, sum1 = 0.0f;
                 // p = 2^(s * scale * log2e - m) with paired fp32 FMAs; P as bf16 pairs over
                 // the first 64 columns of S_t
                 const uint64_t scale2 = f2pack(sl2, sl2);
                 const uint64_t nbase2 = f2pack(-base, -base);
                 uint64_t sum2 = f2pack(0.0f, 0.0f);
+                if constexpr (FP8) {
+                    // P as E4M3, four keys per 32-bit TMEM column (the first 32 columns of S_t);
+                    // p = 2^6 * 2^(s - m) <= 2^8 (max moved at a 4x rise), inside E4M3's range (448)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[BN / 4];
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int c = h * BN / 2; c < (h + 1) * BN / 2; c += 2) {
-                        float t0, t1;
-                        f2unpack(f2fma(f2pack(s[c], s[c + 1]), scale2, nbase2), t0, t1);
-                        const float p0 = ex2_approx(t0);
-                        const float p1 = ex2_approx(t1);
-                        sum2 = f2add(sum2, f2pack(p0, p1));
-                        pk[(c - h * BN / 2) / 2] = pack_bf16x2(p0, p1);
+                        for (int c = h * BN / 2; c < (h + 1) * BN / 2; c += 4) {
+                            float t0, t1, t2, t3;
+                            f2unpack(f2fma(f2pack(s[c], s[c + 1]), scale2, nbase2), t0, t1);
+                            f2unpack(f2fma(f2pack(s[c + 2], s[c + 3]), scale2, nbase2), t2, t3);
+                            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+                            const float p2 = ex2_approx(t2), p3 = ex2_approx(t3);
+                            sum2 = f2add(sum2, f2add(f2pack(p0, p1), f2pack(p2, p3)));
+                            pk[(c - h * BN / 2) / 4] = pack_e4m3x4(p0, p1, p2, p3);
+                        }
+                        tmem_st16(s_tmem + 16 * h, pk);
                     }
-                    tmem_st32(s_tmem + 32 * h, pk);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[BN / 4];
+#pragma unroll
+                        for (int c = h * BN / 2; c < (h + 1) * BN / 2; c += 2) {
+                            float t0, t1;
+                            f2unpack(f2fma(f2pack(s[c], s[c + 1]), scale2, nbase2), t0, t1);
+                            const float p0 = ex2_approx(t0);
+                            const float p1 = ex2_approx(t1);
+                            sum2 = f2add(sum2, f2pack(p0, p1));
+                            pk[(c - h * BN / 2) / 2] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st32(s_tmem + 32 * h, pk);
+                    }
                 }
                 f2unpack(sum2, sum0, sum1);
                 l = l * alpha + (sum0 + sum1);
@@ -741,7 +793,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (T.rows > 0 && ok) {
             const bool valid_row = row < nq;
             const size_t row_idx = (static_cast<size_t>(b) * p.Hq + T.head) * p.Nq + row;
-            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            const float inv_l = l > 0.0f ? p.out_scale / l : 0.0f;
             if (tile_has) {
                 if (mbar_wait(o_done(t), 0, abort_flag, p.err)) {
                     tc_fence_after();
@@ -767,7 +819,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             }
                         }
                     }
-                    if (valid_row) p.lse[row_idx] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                    if (valid_row)
+                        p.lse[row_idx] = l > 0.0f ? (m + log2f(l) - (FP8 ? kFp8PShift : 0.0f)) * kLn2 : -INFINITY;
                 }
             } else if (valid_row) {
                 // no key is allowed for any row of this tile
@@ -838,6 +891,7 @@ int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* ls
     prm.row_ptr = row_ptr;
     prm.col_idx = col_idx;
     prm.next_stride = sm_count();  // one block per SM: the block launched next is about this far on
+    prm.out_scale = 1.0f;
     prm.err = err;
     const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
@@ -855,6 +909,73 @@ int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* ls
                              C::kSmemBytes) != cudaSuccess)
         return kErrCuda;
     attn_fwd_sm103<D, kModeDense><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+}
+
+// FP8 prefill (d = 128): q [B][Hq][Nq][128], k [B][Hkv][Nk][128] and vt [B][Hkv][128][Nk]
+// as E4M3 bytes, read through 8-bit TMA views with 128 x 128-byte boxes (a Q/K tile is
+// 128 rows of 128 bytes; a V^T tile is the 128 d rows of 128 keys). Arguments are already
+// validated (Nk a multiple of 16: the V^T row stride must be 16-byte aligned).
+int launch_fwd_fp8_128(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, float scale, float q_descale, float k_descale, float v_descale, int causal,
+                       int window, cudaStream_t stream, unsigned* err)
+{
+    constexpr int D = 128;
+    using C = FwdCfg<D, 1>;
+    CUtensorMap tq, tk, tv;
+    const uint32_t box[3] = {128u, 128u, 1u};
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nq), static_cast<uint64_t>(B) * Hq};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nq) * D};
+        int rc = encode_u8_map(&tq, q, 3, dims, strides, box);
+        if (rc != kOk) return rc;
+    }
+    if (Nk > 0) {
+        const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nk), static_cast<uint64_t>(B) * Hkv};
+        const uint64_t strides[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Nk) * D};
+        int rc = encode_u8_map(&tk, k, 3, dims, strides, box);
+        if (rc != kOk) return rc;
+        const uint64_t vdims[3] = {static_cast<uint64_t>(Nk), static_cast<uint64_t>(D), static_cast<uint64_t>(B) * Hkv};
+        const uint64_t vstrides[2] = {static_cast<uint64_t>(Nk), static_cast<uint64_t>(D) * Nk};
+        rc = encode_u8_map(&tv, vt, 3, vdims, vstrides, box);
+        if (rc != kOk) return rc;
+    } else {
+        tk = tq;  // no keys: never loaded
+        tv = tq;
+    }
+    FwdParams prm;
+    prm.o = static_cast<__nv_bfloat16*>(o);
+    prm.lse = lse;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.Nq = Nq;
+    prm.Nk = Nk;
+    prm.G = Hq / Hkv;
+    // S comes out of the MMA in code units: the scales of Q and K join the softmax scale
+    prm.scale_log2 = scale * q_descale * k_descale * kLog2e;
+    prm.causal = causal ? 1 : 0;
+    prm.window = window < 0 ? -1 : window;
+    prm.pair_heads = (prm.G % 2 == 0) ? 1 : 0;
+    const int n_row_tiles = (Nq + BM - 1) / BM;
+    prm.n_row_units = prm.pair_heads ? n_row_tiles : (n_row_tiles + 1) / 2;
+    prm.n_hunits = prm.pair_heads ? Hq / 2 : Hq;
+    prm.block_table = nullptr;
+    prm.q_lens = nullptr;
+    prm.kv_lens = nullptr;
+    prm.max_blocks = prm.block_size = prm.bs_log2 = prm.num_blocks = 0;
+    prm.row_ptr = nullptr;
+    prm.col_idx = nullptr;
+    prm.next_stride = sm_count();
+    prm.out_scale = v_descale;
+    prm.err = err;
+    const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
+    if (grid <= 0) return kOk;
+    if (grid > INT_MAX) return kErrInvalidArg;
+    if (cudaFuncSetAttribute(attn_fwd_sm103<D, kModeFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+        return kErrCuda;
+    attn_fwd_sm103<D, kModeFp8><<<static_cast<unsigned>(grid), kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
     return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 
@@ -911,6 +1032,7 @@ int launch_fwd_paged_d(const void* q, const void* k_cache, const void* v_cache, 
     prm.n_row_units = prm.pair_heads ? n_row_tiles : (n_row_tiles + 1) / 2;
     prm.n_hunits = prm.pair_heads ? Hq / 2 : Hq;
     prm.next_stride = 0;
+    prm.out_scale = 1.0f;
     prm.err = err;
     const long long grid = static_cast<long long>(S) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
@@ -949,6 +1071,15 @@ int launch_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
         return launch_fwd_d<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, row_ptr, col_idx, stream,
                                 err);
     return kErrUnsupported;
+}
+
+int launch_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                   int Nk, int d, float scale, float q_descale, float k_descale, float v_descale, int causal,
+                   int window, cudaStream_t stream, unsigned* err)
+{
+    if (d != 128) return kErrUnsupported;
+    return launch_fwd_fp8_128(q, k, vt, o, lse, B, Hq, Hkv, Nq, Nk, scale, q_descale, k_descale, v_descale, causal,
+                              window, stream, err);
 }
 
 int launch_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,

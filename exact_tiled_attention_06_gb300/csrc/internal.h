@@ -37,6 +37,9 @@ int encode_f32_map(CUtensorMap* map, const void* base, int rank, const uint64_t*
 int check_device(int* dev_out);
 // Number of SMs of the current device (0 on failure), looked up once per device.
 int sm_count();
+// Encode a tiled TMA descriptor over an 8-bit tensor (E4M3 bytes) with the 128-byte swizzle.
+int encode_u8_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                  const uint32_t* box);
 // Device address of the library's error word on the current device (nullptr on failure).
 unsigned* device_error_word();
 
@@ -45,6 +48,11 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nq, int Nk, int d, float scale, int causal, int window, cudaStream_t stream,
                unsigned* err);
 
+// FP8 prefill (implemented in fwd_kernel.cu): E4M3 q, k and transposed v, per-tensor
+// scales; d = 128. Arguments are already validated.
+int launch_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                   int Nk, int d, float scale, float q_descale, float k_descale, float v_descale, int causal,
+                   int window, cudaStream_t stream, unsigned* err);
 // Block-sparse prefill (implemented in fwd_kernel.cu): 128 x 128 blocks listed in CSR form
 // (row_ptr [ceil(Nq / 128) + 1], col_idx), device pointers. Arguments are already validated.
 constexpr int kSparseMaxKeys = 2048 * 128;  // the merged walk holds 4096 entries

@@ -233,6 +233,28 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms.
 //   lbo: byte distance between atoms along the leading dimension
 //   sbo: byte distance between 8-row groups along the strided dimension
+// kind::f8f6f4 forms (8-bit E4M3 operands, fp32 accumulator): one instruction covers a
+// K extent of 32 elements (32 bytes).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
 {
     uint64_t d = 0;
@@ -245,6 +267,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, dense.
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0), fp32
+// accumulator, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4)                                   // accumulator format: fp32
+           | (0u << 7)                                 // A format: E4M3
+           | (0u << 10)                                // B format: E4M3
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major)
 {
     return (1u << 4)                                   // accumulator format: fp32
@@ -364,6 +396,16 @@ __device__ __forceinline__ float ex2_approx(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Four floats to four E4M3 codes (round to nearest even, saturating at +-448), the first
+// in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3)
+{
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(a3), "f"(a2));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)

@@ -241,6 +241,37 @@ def decode_config_inputs(cfg: DecodeConfig, seed=None, poison=False):
                          extra_blocks=cfg.extra_blocks, poison=poison)
 
 
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor E4M3 quantisation: scale = max|x| / 448 (1 for an all-zero tensor), codes =
+    x / scale cast to torch's float8_e4m3fn (round to nearest even). Returns (uint8 codes,
+    scale) with x ~ codes * scale."""
+    amax = float(x.abs().max()) if x.numel() else 0.0
+    scale = amax / 448.0 if amax > 0 else 1.0
+    codes = (x.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), scale
+
+
+@dataclass
+class Fp8PrefillInputs:
+    q8: torch.Tensor    # E4M3 codes [B][Hq][Nq][d]
+    k8: torch.Tensor    # E4M3 codes [B][Hkv][Nk][d]
+    vt8: torch.Tensor   # E4M3 codes [B][Hkv][d][Nk] (V transposed)
+    q_descale: float
+    k_descale: float
+    v_descale: float
+
+
+def fp8_prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=0, k_boost_frac=0.0):
+    """The prefill recipe (N(0,1) -> bf16, optional K boost) quantised per tensor to E4M3;
+    V is handed over transposed."""
+    q, k, v = prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=seed, k_boost_frac=k_boost_frac)
+    q8, qs = quantize_e4m3(q)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    return Fp8PrefillInputs(q8=q8, k8=k8, vt8=v8.transpose(-1, -2).contiguous(), q_descale=qs, k_descale=ks,
+                            v_descale=vs)
+
+
 @dataclass(frozen=True)
 class DecodeStepConfig:
     """One decode step of an n-layer model: every layer has its own cache and queries; the

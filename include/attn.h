@@ -73,6 +73,37 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int causal, int window, void* stream);
 
 /*
+ * attn_fwd_fp8 -- prefill attention over 8-bit E4M3 Q, K and V with per-tensor scales.
+ *
+ *   AK, the FlashAttention-3 paragraph (FP8 operands), with the tiled online-softmax
+ *   computation of attn_fwd. The real inputs are Q = q_descale * q, K = k_descale * k and
+ *   V = v_descale * v, where q, k, v hold E4M3 codes (OCP 8-bit floating point: sign,
+ *   4-bit exponent with bias 7, 3-bit mantissa, subnormals, one NaN code per sign, no
+ *   infinity). O and lse are those of attn_fwd on these real inputs with one extra
+ *   rounding: each unnormalised probability, held as p = 2^6 * 2^(s - m) with m a
+ *   running maximum that lags the true one by less than a factor 4 (so p <= 2^8), is
+ *   rounded to E4M3 for the P V product (nearest even: relative error at most 2^-4 for
+ *   p >= 2^-6, i.e. probabilities down to 2^-12 of the row maximum's weight; absolute
+ *   error at most 2^-10 in p below), while the row sum uses the unrounded values.
+ *
+ *   q  : E4M3 bytes [B][Hq][Nq][128]      (input)
+ *   k  : E4M3 bytes [B][Hkv][Nk][128]     (input)
+ *   vt : E4M3 bytes [B][Hkv][128][Nk]     (input) V transposed: element (key j, column t)
+ *                                          of kv head h is vt[h][t][j]
+ *   o  : bf16 [B][Hq][Nq][128]            (output)
+ *   lse: fp32 [B][Hq][Nq]                 (output) as attn_fwd
+ *   scale, causal, window, B, Hq, Hkv, Nq, Nk: as attn_fwd. q_descale, k_descale,
+ *   v_descale: > 0 and finite (else ATTN_ERR_INVALID_ARG). d must be 128 and Nk a
+ *   multiple of 16 (the V^T rows must stay 16-byte aligned); otherwise
+ *   ATTN_ERR_UNSUPPORTED. NaN codes in the inputs propagate as in any IEEE arithmetic.
+ *   Enqueues one kernel on `stream`. Returns ATTN_OK or a negative attn_status.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse,
+                 int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                 float q_descale, float k_descale, float v_descale,
+                 int causal, int window, void* stream);
+
+/*
  * attn_fwd_blocksparse -- prefill restricted to the 128 x 128 score blocks a block index
  * lists.
  *

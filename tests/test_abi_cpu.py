@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_expected_entry_points():
@@ -151,6 +151,25 @@ def dec(lib, ws_bytes=None, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, o=FAKE, 
     if ws_bytes is None:
         ws_bytes = lib.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb)
     return lib.attn_decode(q, kc, vc, bt, sl, o, lse, S, Hq, Hkv, d, bs, mb, nb, scale, ws, ws_bytes, None)
+
+
+def fp8(lib, q=FAKE, k=FAKE, vt=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=1, Nq=8, Nk=16, d=128, scale=0.1, qs=0.01,
+        ks=0.01, vs=0.01, causal=0, window=-1):
+    return lib.attn_fwd_fp8(q, k, vt, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, qs, ks, vs, causal, window, None)
+
+
+def test_fp8_argument_validation(lib):
+    assert fp8(lib, q=None) == -1
+    assert fp8(lib, vt=None) == -1
+    assert fp8(lib, vt=None, k=None, Nk=0, Nq=0) == 0   # no keys: k and vt are never read
+    assert fp8(lib, Hq=3, Hkv=2) == -1
+    assert fp8(lib, qs=0.0) == -1
+    assert fp8(lib, ks=float("inf")) == -1
+    assert fp8(lib, vs=-1.0) == -1
+    assert fp8(lib, d=64) == -2                        # d = 128 only
+    assert fp8(lib, Nk=100) == -2                      # V^T rows must stay 16-byte aligned
+    assert fp8(lib, vt=FAKE + 8) == -3
+    assert fp8(lib, Nq=0) == 0                         # nothing to compute: no launch
 
 
 def test_decode_argument_validation(lib):
