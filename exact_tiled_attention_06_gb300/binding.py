@@ -27,7 +27,7 @@ STATUS_NAMES = {
 EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
             "attn_decode_noalloc", "attn_decode_graph_create", "attn_decode_graph_launch", "attn_decode_graph_layers",
-            "attn_decode_graph_destroy")
+            "attn_decode_graph_destroy", "attn_fwd_host", "attn_decode_host")
 
 
 class AttnError(RuntimeError):
@@ -88,6 +88,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_decode_graph_layers.restype = i
         lib.attn_decode_graph_destroy.argtypes = [vp]
         lib.attn_decode_graph_destroy.restype = i
+        lib.attn_fwd_host.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, i, i, i, vp]
+        lib.attn_fwd_host.restype = i
+        lib.attn_decode_host.argtypes = [vp] * 14 + [i, i, i, i, i, i, i, f, vp, sz, vp]
+        lib.attn_decode_host.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -440,3 +444,72 @@ def attn_decode_graph_create(qs, k_caches, v_caches, block_table, seq_lens, scal
         raise AttnError(rc, "attn_decode_graph_create")
     return DecodeGraph(h.value, (list(qs), list(k_caches), list(v_caches), block_table, seq_lens, workspace),
                        outs, lses)
+
+
+def _need_host(t, name: str, dtype: torch.dtype, ndim: int):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor with {ndim} dimensions")
+
+
+def attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, causal=False, window=-1, scale=None,
+                  chunk_kv_heads=0, stream=None):
+    """attn_fwd from host tensors (pinned for overlap): the inputs are copied into the device
+    tensors *_d chunk by chunk while earlier chunks compute and copy back into o_h / lse_h.
+    Returns (o_h, lse_h); complete when ``stream`` is."""
+    for n, t, nd in (("q_h", q_h, 4), ("k_h", k_h, 4), ("v_h", v_h, 4), ("o_h", o_h, 4)):
+        _need_host(t, n, torch.bfloat16, nd)
+    _need_host(lse_h, "lse_h", torch.float32, 3)
+    for n, t in (("q_d", q_d), ("k_d", k_d), ("v_d", v_d), ("o_d", o_d)):
+        _need(t, n, torch.bfloat16, 4)
+    _need(lse_d, "lse_d", torch.float32, 3)
+    B, Hq, Nq, d = q_h.shape
+    Bk, Hkv, Nk, dk = k_h.shape
+    if (Bk != B or dk != d or v_h.shape != k_h.shape or q_d.shape != q_h.shape or k_d.shape != k_h.shape
+            or v_d.shape != v_h.shape or o_h.shape != q_h.shape or o_d.shape != q_h.shape
+            or tuple(lse_h.shape) != (B, Hq, Nq) or lse_d.shape != lse_h.shape):
+        raise ValueError("host / device shapes disagree")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load_library().attn_fwd_host(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(lse_h), _ptr(q_d), _ptr(k_d),
+                                      _ptr(v_d), _ptr(o_d), _ptr(lse_d), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                                      int(bool(causal)), int(window), int(chunk_kv_heads), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
+    return o_h, lse_h
+
+
+def attn_decode_host(q_h, k_cache_h, v_cache_h, block_table_h, seq_lens_h, o_h, lse_h, q_d, k_cache_d, v_cache_d,
+                     block_table_d, seq_lens_d, o_d, lse_d, scale=None, workspace=None, stream=None):
+    """attn_decode from host tensors: everything is copied in, decoded and copied back in
+    order on ``stream``. Returns (o_h, lse_h); complete when ``stream`` is."""
+    _need_host(q_h, "q_h", torch.bfloat16, 3)
+    _need_host(k_cache_h, "k_cache_h", torch.bfloat16, 4)
+    _need_host(v_cache_h, "v_cache_h", torch.bfloat16, 4)
+    _need_host(block_table_h, "block_table_h", torch.int32, 2)
+    _need_host(seq_lens_h, "seq_lens_h", torch.int32, 1)
+    _need_host(o_h, "o_h", torch.bfloat16, 3)
+    _need_host(lse_h, "lse_h", torch.float32, 2)
+    S, Hq, d = q_h.shape
+    nb, Hkv, bs, _ = k_cache_h.shape
+    mb = block_table_h.shape[1]
+    for n, t, ref in (("q_d", q_d, q_h), ("k_cache_d", k_cache_d, k_cache_h), ("v_cache_d", v_cache_d, v_cache_h),
+                      ("block_table_d", block_table_d, block_table_h), ("seq_lens_d", seq_lens_d, seq_lens_h),
+                      ("o_d", o_d, o_h), ("lse_d", lse_d, lse_h)):
+        _need(t, n, ref.dtype, ref.dim())
+        if t.shape != ref.shape:
+            raise ValueError(f"{n} shape differs from its host tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_d.device)
+    rc = load_library().attn_decode_host(_ptr(q_h), _ptr(k_cache_h), _ptr(v_cache_h), _ptr(block_table_h),
+                                         _ptr(seq_lens_h), _ptr(o_h), _ptr(lse_h), _ptr(q_d), _ptr(k_cache_d),
+                                         _ptr(v_cache_d), _ptr(block_table_d), _ptr(seq_lens_d), _ptr(o_d),
+                                         _ptr(lse_d), S, Hq, Hkv, d, bs, mb, nb, float(scale), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_host")
+    return o_h, lse_h

@@ -330,6 +330,40 @@ int attn_decode_graph_layers(const void* graph);
 int attn_decode_graph_destroy(void* graph);
 
 /*
+ * attn_fwd_host / attn_decode_host -- attn_fwd and attn_decode from HOST buffers: the
+ * copies to the device and back are part of the call.
+ *
+ *   No counterpart in the pages: the end-to-end entry points of the library.
+ *   The *_h arguments are host pointers, the *_d arguments device buffers of the same
+ *   shapes and layouts (the caller owns both; inputs are copied into the *_d buffers, the
+ *   outputs computed there and copied back to the *_h buffers). Page-locked host memory
+ *   (cudaHostAlloc / cudaHostRegister) is needed for the copies to overlap anything; with
+ *   pageable memory the result is the same and the copies are synchronous. Sizes, scale,
+ *   masks, workspace and errors are those of attn_fwd / attn_decode; d_* pointers must meet
+ *   their alignment rules. Everything is ordered after the work already queued on `stream`
+ *   and complete on `stream` when the last copy back is; the host buffers must stay valid
+ *   and unchanged until then. The results are bitwise those of attn_fwd / attn_decode.
+ *
+ *   attn_fwd_host pipelines chunks of chunk_kv_heads kv heads (with their query heads) of
+ *   one batch entry over the library's two copy streams (created on first use, per device,
+ *   kept until exit) and `stream`: chunk c+1 is copied in while chunk c is computed and
+ *   chunk c-1 is copied out. chunk_kv_heads <= 0 picks max(1, Hkv / 4).
+ *   attn_decode_host copies q, the block table, the lengths and both caches in, runs the
+ *   decode, and copies O and lse out, all in order on `stream` (the decode reads the whole
+ *   cache, so there is nothing to overlap within one call).
+ */
+int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                  void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
+                  int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal, int window,
+                  int chunk_kv_heads, void* stream);
+int attn_decode_host(const void* q_h, const void* k_cache_h, const void* v_cache_h,
+                     const int32_t* block_table_h, const int32_t* seq_lens_h, void* o_h, float* lse_h,
+                     void* q_d, void* k_cache_d, void* v_cache_d, int32_t* block_table_d,
+                     int32_t* seq_lens_d, void* o_d, float* lse_d, int num_seqs, int Hq, int Hkv, int d,
+                     int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_chunk_tokens -- keys per split-KV chunk attn_decode uses for these sizes
  * (AK FlashDecoding: the chunk length of the split). 512 keys, halved (down to 128, and
  * staying a multiple of block_size) while the work items -- chunks of the longest

@@ -172,6 +172,27 @@ def test_fp8_argument_validation(lib):
     assert fp8(lib, Nq=0) == 0                         # nothing to compute: no launch
 
 
+def test_host_entry_points_validation(lib):
+    F = FAKE
+    fh = lambda **kw: lib.attn_fwd_host(*(kw.get(n, F) for n in ("qh", "kh", "vh", "oh", "lh", "qd", "kd", "vd", "od",
+                                                                  "ld")), 1, 2, 1, kw.get("Nq", 8), 16,
+                                        kw.get("d", 128), 0.1, 0, -1, 0, None)
+    assert fh(qh=None) == -1
+    assert fh(kd=None) == -1
+    assert fh(d=80) == -2
+    assert fh(od=F + 8) == -3
+    assert fh(Nq=0, qh=None, oh=None, lh=None, qd=None, od=None, ld=None) == 0
+    ws = lib.attn_decode_workspace_size(4, 8, 2, 128, 16, 64)
+    dh = lambda **kw: lib.attn_decode_host(*(kw.get(n, F) for n in ("qh", "kh", "vh", "bh", "sh", "oh", "lh", "qd",
+                                                                     "kd", "vd", "bd", "sd", "od", "ld")), 4, 8, 2,
+                                           kw.get("d", 128), kw.get("bs", 16), 64, 256, 0.1, F, kw.get("wsb", ws), None)
+    assert dh(sh=None) == -1
+    assert dh(vd=None) == -1
+    assert dh(bs=24) == -2
+    assert dh(ld=F + 2) == -3
+    assert dh(wsb=16) == -4
+
+
 def test_decode_argument_validation(lib):
     assert dec(lib, q=None) == -1
     assert dec(lib, bt=None) == -1
