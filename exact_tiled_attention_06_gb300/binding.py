@@ -27,7 +27,8 @@ STATUS_NAMES = {
 EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_prefill_paged", "attn_bwd_workspace_size", "attn_bwd", "attn_decode_workspace_size", "attn_decode",
             "attn_decode_chunk_tokens", "attn_get_device_error", "attn_kv_layout_version", "attn_status_string",
             "attn_decode_noalloc", "attn_decode_graph_create", "attn_decode_graph_launch", "attn_decode_graph_layers",
-            "attn_decode_graph_destroy", "attn_fwd_host", "attn_decode_host")
+            "attn_decode_graph_destroy", "attn_fwd_host", "attn_decode_host",
+            "attn_selftest_wait_timeout")
 
 
 class AttnError(RuntimeError):
@@ -92,6 +93,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.attn_fwd_host.restype = i
         lib.attn_decode_host.argtypes = [vp] * 14 + [i, i, i, i, i, i, i, f, vp, sz, vp]
         lib.attn_decode_host.restype = i
+        lib.attn_selftest_wait_timeout.argtypes = [vp]
+        lib.attn_selftest_wait_timeout.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -513,3 +516,11 @@ def attn_decode_host(q_h, k_cache_h, v_cache_h, block_table_h, seq_lens_h, o_h, 
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_host")
     return o_h, lse_h
+
+
+def attn_selftest_wait_timeout(stream=None) -> None:
+    """Launch a block whose barrier wait runs out (about 2 s); the device error word then
+    reads ATTN_ERR_DEVICE_TIMEOUT. For failure-detection tests."""
+    rc = load_library().attn_selftest_wait_timeout(_stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_selftest_wait_timeout")

@@ -364,6 +364,16 @@ int attn_decode_host(const void* q_h, const void* k_cache_h, const void* v_cache
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_selftest_wait_timeout -- failure detection without a fault: launches one block
+ * whose pipeline-barrier wait is never satisfied. The wait gives up after its time limit
+ * (about 2 s, as every wait in the library) and records ATTN_ERR_DEVICE_TIMEOUT in the
+ * device error word; attn_get_device_error() then returns it, and the context stays
+ * usable. For tests of the error path; nothing else calls it. Enqueues one kernel on
+ * `stream`; returns ATTN_OK or a negative attn_status.
+ */
+int attn_selftest_wait_timeout(void* stream);
+
+/*
  * attn_decode_chunk_tokens -- keys per split-KV chunk attn_decode uses for these sizes
  * (AK FlashDecoding: the chunk length of the split). 512 keys, halved (down to 128, and
  * staying a multiple of block_size) while the work items -- chunks of the longest

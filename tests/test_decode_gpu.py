@@ -172,3 +172,18 @@ def test_counters_left_at_zero_for_the_next_call():
     n_ctr = 16 + 4 * 6 * 2  # claim counter, exit counter and pad, one completion counter per (seq, kv head)
     torch.cuda.synchronize()
     assert int(ws[:n_ctr].count_nonzero()) == 0
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A barrier wait that nothing completes gives up after its time limit: the host reads
+    ATTN_ERR_DEVICE_TIMEOUT, the read clears it, and the next calls run normally."""
+    from exact_tiled_attention_06_gb300 import binding
+    binding.attn_selftest_wait_timeout()
+    assert eta.attn_get_device_error() == -6
+    assert eta.attn_get_device_error() == 0
+    x = inputs.decode_inputs(3, 8, 2, 128, 16, len_lo=1, len_hi=500, seed=60)
+    run_decode(x, 1.0 / math.sqrt(128))
+    q, k, v = [t.cuda() for t in inputs.prefill_inputs(1, 2, 1, 130, 130, 64, seed=61)]
+    eta.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert eta.attn_get_device_error() == 0
