@@ -391,7 +391,7 @@ int attn_decode_chunk_tokens(int num_seqs, int Hq, int Hkv, int block_size, int 
 int attn_get_device_error(void* stream);
 
 /*
- * attn_kv_layout_version -- identity of the paged-cache layout this build reads
+ * attn_kv_layout_version -- identity of the paged-cache layout the library reads
  * (MAK "Failure modes", page-table mismatch: encode layout identity).
  * Version 1 = [num_blocks][Hkv][block_size][d], bf16, block_table int32 row-major.
  */
