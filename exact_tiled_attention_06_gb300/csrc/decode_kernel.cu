@@ -287,21 +287,25 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 phys = 0;
             }
         }
-        // Issue the TMA copies of sub-page i of this item into its ring stage.
-        auto issue = [&](int i) {
-            const int tok = tok0 + i * kSub;
+        // Cache row of every sub-page of the item, one per lane (n_sub <= 32): the first
+        // row of its 16 tokens in the [block][kv head][token] row space.
+        int sub_row = 0;
+        {
+            const int tok = tok0 + min(lane, n_sub - 1) * kSub;
             const int lb = tok / p.block_size;
             const int ph = __shfl_sync(0xffffffffu, phys, lb - lb0);
+            sub_row = (ph * p.Hkv + hkv) * p.block_size + (tok - lb * p.block_size);
+        }
+        // Issue the TMA copies of sub-page i of this item into its ring stage: one copy for
+        // K and one for V, each landing as kBoxes 16-row boxes of 128 bytes.
+        auto issue = [&](int i) {
+            const int row = __shfl_sync(0xffffffffu, sub_row, i);
             if (lane == 0) {
-                const int row = (ph * p.Hkv + hkv) * p.block_size + (tok - lb * p.block_size);
                 const int s = static_cast<int>((uses + i) % C::kStages);
                 const uint32_t dst = ring + s * C::kStageBytes;
                 mbar_arrive_expect_tx(full(s), C::kStageBytes);
-#pragma unroll
-                for (int x = 0; x < C::kBoxes; ++x) tma_load_2d(dst + x * C::kBoxBytes, &tm_k, full(s), 64 * x, row);
-#pragma unroll
-                for (int x = 0; x < C::kBoxes; ++x)
-                    tma_load_2d(dst + C::kSubBytes + x * C::kBoxBytes, &tm_v, full(s), 64 * x, row);
+                tma_load_3d(dst, &tm_k, full(s), 0, row, 0);
+                tma_load_3d(dst + C::kSubBytes, &tm_v, full(s), 0, row, 0);
             }
         };
         const int primed = min(C::kStages, n_sub);
@@ -353,16 +357,22 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 __syncwarp();
             }
             // ---- S = q K^T (16 heads x 16 tokens)
+            // (even and odd k steps accumulate separately: four short chains, not two long)
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int U = 2 * kk + k_unit;
                 const uint32_t addr = sK + (U >> 3) * C::kBoxBytes + k_token * 128 + (((U & 7) ^ rr) << 4);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(addr, b0, b1, b2, b3);
-                mma_16816(sc[0], qa[kk], b0, b1);
-                mma_16816(sc[1], qa[kk], b2, b3);
+                mma_16816((kk & 1) ? sd[0] : sc[0], qa[kk], b0, b1);
+                mma_16816((kk & 1) ? sd[1] : sc[1], qa[kk], b2, b3);
             }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
             if (ntok < kSub) {
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -470,67 +480,116 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         if (!last) continue;
         // ---- this warp finished the last chunk of (seq, head group): merge every partial.
         // Eight lanes per query head (four heads at a time), each lane owning D/8
-        // consecutive columns: the log-sums of a head are reduced over its eight lanes, and
-        // the partial rows are read four chunks at a time with independent 16-byte loads,
-        // so that many loads are in flight instead of one chain per chunk.
+        // consecutive columns. The chunks' log-sums are spread over a head's eight lanes
+        // (chunk c on lane c % 8), kept in registers and reduced there; their weights reach
+        // the other lanes by shuffle. The partial rows are read four chunks at a time with
+        // independent 16-byte loads, the first four issued before the log-sums are reduced.
         __threadfence();
         {
             constexpr int kCols = D / 8;           // columns per lane (16 or 8)
             constexpr int kVec = kCols / 4;        // float4 loads per lane per chunk
+            constexpr int kHeld = 8;               // log-sums per lane: up to 64 chunks in registers
             const int slot_row = lane >> 3;        // head within the group of four
-            const int cg = lane & 7;               // column group
+            const int cg = lane & 7;               // column group (and chunk c = cg mod 8)
             const size_t split_stride = static_cast<size_t>(p.num_seqs) * p.Hq;  // rows per chunk
             for (int rb = 0; rb < nvalid; rb += 4) {
                 const int row = rb + slot_row;
                 const bool live = row < nvalid;
                 const size_t r0 = static_cast<size_t>(seq) * p.Hq + hq0 + (live ? row : nvalid - 1);
                 const float* lse_r = p.part_lse + r0;
-                float M = -INFINITY;
-                for (int c = cg; c < n_splits; c += 8) M = fmaxf(M, __ldcg(lse_r + c * split_stride));
-                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-                float S = 0.0f;
-                for (int c = cg; c < n_splits; c += 8) S += ex2_approx(__ldcg(lse_r + c * split_stride) - M);
-                S += __shfl_xor_sync(0xffffffffu, S, 1);
-                S += __shfl_xor_sync(0xffffffffu, S, 2);
-                S += __shfl_xor_sync(0xffffffffu, S, 4);
+                const float* po = p.part_o + r0 * D + cg * kCols;
                 float acc[kCols];
 #pragma unroll
                 for (int t = 0; t < kCols; ++t) acc[t] = 0.0f;
-                const float* po = p.part_o + r0 * D + cg * kCols;
-                int c = 0;
-                for (; c + 4 <= n_splits; c += 4) {
-                    float lv[4];
-                    float4 v[4][kVec];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        lv[k] = __ldcg(lse_r + (c + k) * split_stride);
-#pragma unroll
-                        for (int x = 0; x < kVec; ++x)
-                            v[k][x] = __ldcg(reinterpret_cast<const float4*>(po + (c + k) * split_stride * D) + x);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float w = ex2_approx(lv[k] - M);
-#pragma unroll
-                        for (int x = 0; x < kVec; ++x) {
-                            acc[4 * x + 0] = fmaf(w, v[k][x].x, acc[4 * x + 0]);
-                            acc[4 * x + 1] = fmaf(w, v[k][x].y, acc[4 * x + 1]);
-                            acc[4 * x + 2] = fmaf(w, v[k][x].z, acc[4 * x + 2]);
-                            acc[4 * x + 3] = fmaf(w, v[k][x].w, acc[4 * x + 3]);
-                        }
-                    }
-                }
-                for (; c < n_splits; ++c) {
-                    const float w = ex2_approx(__ldcg(lse_r + c * split_stride) - M);
+                auto add4 = [&](const float4 (&v)[kVec], float w) {
 #pragma unroll
                     for (int x = 0; x < kVec; ++x) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4*>(po + c * split_stride * D) + x);
-                        acc[4 * x + 0] = fmaf(w, v.x, acc[4 * x + 0]);
-                        acc[4 * x + 1] = fmaf(w, v.y, acc[4 * x + 1]);
-                        acc[4 * x + 2] = fmaf(w, v.z, acc[4 * x + 2]);
-                        acc[4 * x + 3] = fmaf(w, v.w, acc[4 * x + 3]);
+                        acc[4 * x + 0] = fmaf(w, v[x].x, acc[4 * x + 0]);
+                        acc[4 * x + 1] = fmaf(w, v[x].y, acc[4 * x + 1]);
+                        acc[4 * x + 2] = fmaf(w, v[x].z, acc[4 * x + 2]);
+                        acc[4 * x + 3] = fmaf(w, v[x].w, acc[4 * x + 3]);
+                    }
+                };
+                float M = -INFINITY, S = 0.0f;
+                if (n_splits <= 8 * kHeld) {
+                    // first four chunks' rows (n_splits >= 2), then the log-sums, all in flight
+                    const int c0n = min(4, n_splits);
+                    float4 v0[4][kVec];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int x = 0; x < kVec; ++x)
+                            v0[k][x] = k < c0n ? __ldcg(reinterpret_cast<const float4*>(po + k * split_stride * D) + x)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float hl[kHeld];
+#pragma unroll
+                    for (int k = 0; k < kHeld; ++k) {
+                        const int c = cg + 8 * k;
+                        hl[k] = c < n_splits ? __ldcg(lse_r + c * split_stride) : -INFINITY;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kHeld; ++k) M = fmaxf(M, hl[k]);
+                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+#pragma unroll
+                    for (int k = 0; k < kHeld; ++k) {
+                        hl[k] = ex2_approx(hl[k] - M);  // the chunk's weight (0 past n_splits)
+                        S += hl[k];
+                    }
+                    S += __shfl_xor_sync(0xffffffffu, S, 1);
+                    S += __shfl_xor_sync(0xffffffffu, S, 2);
+                    S += __shfl_xor_sync(0xffffffffu, S, 4);
+                    const int src0 = slot_row * 8;  // the lane holding chunk 8k + 0 of this head
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) add4(v0[k], __shfl_sync(0xffffffffu, hl[0], src0 + k));
+#pragma unroll
+                    for (int kb = 0; kb < kHeld; ++kb) {
+                        // chunks 8 kb .. 8 kb + 7, four at a time (0..3 of kb = 0 are done)
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const int c = 8 * kb + 4 * half;
+                            if (c == 0) continue;
+                            if (c >= n_splits) break;
+                            const int cn = min(4, n_splits - c);
+                            float4 v[4][kVec];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                                for (int x = 0; x < kVec; ++x)
+                                    v[k][x] = k < cn
+                                        ? __ldcg(reinterpret_cast<const float4*>(po + (c + k) * split_stride * D) + x)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                add4(v[k], __shfl_sync(0xffffffffu, hl[kb], src0 + 4 * half + k));
+                        }
+                    }
+                } else {
+                    // more chunks than registers hold: log-sums read twice, rows four at a time
+                    for (int c = cg; c < n_splits; c += 8) M = fmaxf(M, __ldcg(lse_r + c * split_stride));
+                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+                    for (int c = cg; c < n_splits; c += 8) S += ex2_approx(__ldcg(lse_r + c * split_stride) - M);
+                    S += __shfl_xor_sync(0xffffffffu, S, 1);
+                    S += __shfl_xor_sync(0xffffffffu, S, 2);
+                    S += __shfl_xor_sync(0xffffffffu, S, 4);
+                    for (int c = 0; c < n_splits; c += 4) {
+                        const int cn = min(4, n_splits - c);
+                        float lv[4];
+                        float4 v[4][kVec];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            lv[k] = k < cn ? __ldcg(lse_r + (c + k) * split_stride) : -INFINITY;
+#pragma unroll
+                            for (int x = 0; x < kVec; ++x)
+                                v[k][x] = k < cn
+                                    ? __ldcg(reinterpret_cast<const float4*>(po + (c + k) * split_stride * D) + x)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) add4(v[k], ex2_approx(lv[k] - M));
                     }
                 }
                 if (live) {
@@ -576,14 +635,17 @@ int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, con
     // leaves them at zero again, so a chain of launches needs this only once
     if (!(flags & kDecodeCountersZeroed) && cudaMemsetAsync(ws, 0, plan.counters_bytes, stream) != cudaSuccess)
         return kErrCuda;
+    // The cache as rows of D elements, each row seen as kBoxes 64-column pieces: dims
+    // {column in piece, row, piece}, so that one copy brings a sub-page's 16 rows as kBoxes
+    // boxes of 16 x 128 bytes (piece-major, each box swizzled on its own).
     CUtensorMap tk, tv;
-    const uint64_t dims[2] = {static_cast<uint64_t>(D),
-                              static_cast<uint64_t>(num_blocks) * Hkv * static_cast<uint64_t>(block_size)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(D) * 2};
-    const uint32_t box[2] = {64u, static_cast<uint32_t>(kSub)};
-    int rc = encode_bf16_map(&tk, k_cache, 2, dims, strides, box);
+    const uint64_t dims[3] = {64u, static_cast<uint64_t>(num_blocks) * Hkv * static_cast<uint64_t>(block_size),
+                              static_cast<uint64_t>(C::kBoxes)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, 128u};
+    const uint32_t box[3] = {64u, static_cast<uint32_t>(kSub), static_cast<uint32_t>(C::kBoxes)};
+    int rc = encode_bf16_map(&tk, k_cache, 3, dims, strides, box);
     if (rc != kOk) return rc;
-    rc = encode_bf16_map(&tv, v_cache, 2, dims, strides, box);
+    rc = encode_bf16_map(&tv, v_cache, 3, dims, strides, box);
     if (rc != kOk) return rc;
     const int sms = sm_count();
     if (sms <= 0) return kErrCuda;
