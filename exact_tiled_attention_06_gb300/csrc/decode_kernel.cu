@@ -354,6 +354,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 for (int x = 0; x < C::kBoxes; ++x)
                     for (int u = lane; u < units; u += 32)
                         reinterpret_cast<uint4*>(vrow + x * C::kBoxBytes + ntok * 128)[u] = make_uint4(0u, 0u, 0u, 0u);
+                // these generic-proxy writes precede the stage's next TMA fill
+                fence_proxy_async_smem();
                 __syncwarp();
             }
             // ---- S = q K^T (16 heads x 16 tokens)
@@ -381,15 +383,27 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                         if (8 * nt + 2 * tig + (e & 1) >= ntok) sc[nt][e] = -INFINITY;
             }
             // ---- online softmax per row (rows g: e = 0,1; rows g+8: e = 2,3)
+            float mx[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                mx[h] = fmaxf(fmaxf(sc[0][2 * h], sc[0][2 * h + 1]), fmaxf(sc[1][2 * h], sc[1][2 * h + 1]));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+            bool grow[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                float mx = fmaxf(fmaxf(sc[0][2 * h], sc[0][2 * h + 1]), fmaxf(sc[1][2 * h], sc[1][2 * h + 1]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_cand = mx * sl2;
-                if (m_cand > m[h] + kRescaleThreshold || (m[h] == -INFINITY && m_cand > -INFINITY)) {
-                    const float m_new = fmaxf(m[h], m_cand);
-                    const float alpha = (m[h] == -INFINITY) ? 0.0f : ex2_approx(m[h] - m_new);
+                const float m_cand = mx[h] * sl2;
+                grow[h] = m_cand > m[h] + kRescaleThreshold || (m[h] == -INFINITY && m_cand > -INFINITY);
+                mx[h] = m_cand;
+            }
+            if (grow[0] || grow[1]) {
+                // the running maximum moved by more than the threshold: rescale O and l
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float m_new = grow[h] ? fmaxf(m[h], mx[h]) : m[h];
+                    const float alpha = !grow[h] ? 1.0f : (m[h] == -INFINITY) ? 0.0f : ex2_approx(m[h] - m_new);
                     m[h] = m_new;
                     l[h] *= alpha;
 #pragma unroll
@@ -398,6 +412,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                         o[nt][2 * h + 1] *= alpha;
                     }
                 }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
                 const float base = (m[h] == -INFINITY) ? 0.0f : m[h];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -426,8 +443,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
             }
             __syncwarp();
             if (i + C::kStages < n_sub) {
-                // the stage's generic-proxy reads (and any zeroing) precede the next TMA fill
-                fence_proxy_async_smem();
+                // every read of the stage has returned (the P V products consumed them)
                 issue(i + C::kStages);
                 ++issued;
             }
