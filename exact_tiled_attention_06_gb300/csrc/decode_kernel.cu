@@ -3,8 +3,11 @@
 // One persistent kernel, one block per SM, eight independent worker warps per block.
 // A work item is (key chunk of 512 tokens -- fewer for a small batch, down to 128 -- kv
 // head [, group of 16 query heads], sequence). Each block first reads the sequence
-// lengths (on the device: the host never reads them) and prefix-sums their chunk counts
-// in shared memory, so items exist only inside sequences. Each warp then repeatedly:
+// lengths (on the device: the host never reads them), orders the sequences by chunk
+// count and prefix-sums the counts in shared memory, so items exist only inside
+// sequences. When the launch has at most half as many items as warps, a team of T = 2
+// or 4 warps of a block shares each item (its sub-pages dealt round-robin); otherwise
+// T = 1. Each team then repeatedly:
 //   * takes an item: its own index first, then the next one from a device-wide counter
 //     (items in sequence order -- most chunks first -- then head group, then chunk),
 //   * loads the item's block-table entries (one per lane) and the query heads of its
@@ -14,9 +17,12 @@
 //   * computes S = q K^T and O += P V with mma.sync m16n8k16 (the query heads of the kv
 //     head are the M rows: every K/V byte is read once for the whole group) with a
 //     per-row online softmax in registers,
+//   * (a team) combines its members' partials in shared memory, member w taking the
+//     columns [w D/T, (w + 1) D/T),
 //   * writes the chunk's normalised partial and log-sum; the warp that completes the
-//     last chunk of a (sequence, head group) merges all its partials and writes O and
-//     lse. A sequence that fits in one chunk is written directly.
+//     last chunk of a (sequence, head group) -- per column slice for a team -- merges
+//     all its partials and writes O and lse. A sequence that fits in one chunk is
+//     written directly.
 // Every launch leaves its counters at zero (the merging warp resets its completion
 // counter, the last warp to leave resets the claim counters), and every block signals
 // programmatic dependents at its start and waits for its own predecessor before touching
@@ -52,6 +58,7 @@ constexpr long long kTargetItems = 152 * 8;  // worker warps of a full GB300 (15
 constexpr int kMaxChunkBlocks = 32;   // block-table entries per item (one per lane)
 constexpr int kRowsPerItem = 16;      // query heads per item (mma M)
 constexpr int kPlanMaxSeqs = 2048;    // sequences per launch (the block's length table)
+constexpr int kMaxTeamAll = 4;        // warps sharing an item at most, any head size
 static_assert(kPlanMaxSeqs <= 2048, "the sort key holds the sequence in 11 bits");
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994531f;
@@ -70,8 +77,17 @@ struct DecCfg {
     // lengths, chunk prefix, per-warp scan totals, sequences in heaviest-first order
     static constexpr int kPlanOff = kUsedBytes;
     static constexpr int kPlanBytes = (3 * kPlanMaxSeqs + 2 + kDecWarps) * 4;
-    static constexpr int kSmemBytes = kPlanOff + kPlanBytes + 1024;
+    // teams: claimed item per team (two slots, by iteration parity), abort flags, and
+    // each warp's (m, l) per row for the team's combine
+    static constexpr int kMaxTeam = D / 32;  // warps per item at most (a lane owns >= 4 columns)
+    static_assert(kMaxTeam <= kMaxTeamAll, "completion counters per (sequence, head group)");
+    static constexpr int kTeamOff = kPlanOff + kPlanBytes;
+    static constexpr int kTeamBytes = kDecWarps * 2 * 8 + kDecWarps * 4 + kDecWarps * kRowsPerItem * 8;
+    static constexpr int kRowF = D + 8;      // floats per row of a warp's partial O in its ring
+    static_assert(kRowsPerItem * kRowF * 4 <= kStages * 2 * kBoxes * kBoxBytes, "partial O fits the ring");
+    static constexpr int kSmemBytes = kTeamOff + kTeamBytes + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kTeamOff % 8 == 0, "team area alignment");
 };
 
 struct DecParams {
@@ -144,59 +160,89 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     {
         constexpr int kThreads = kDecWarps * 32;
         const int S = p.num_seqs;
-        int N = 1;
-        while (N < S) N <<= 1;
         // key = (65535 - chunks) << 11 | sequence: ascending keys = most chunks first, ties
         // in sequence order (chunks <= 65535 and sequence < 2048 per launch)
-        for (int i = threadIdx.x; i < N; i += kThreads) {
-            int key = INT_MAX;
+        if (S <= kThreads) {
+            // One sequence per thread: its place in the order and its prefix by counting the
+            // smaller keys (the unsorted keys wait in the upper half of the key array).
+            constexpr int kTmp = kPlanMaxSeqs - kThreads;
+            const int i = threadIdx.x;
+            int key = 0, n = 0;
             if (i < S) {
                 const int L = clamp_len(p, p.seq_lens[i]);
                 sL[i] = L;
-                const int n = L > 0 ? (L + p.chunk - 1) / p.chunk : 1;
+                n = L > 0 ? (L + p.chunk - 1) / p.chunk : 1;
                 key = ((65535 - n) << 11) | i;
+                sKey[kTmp + i] = key;
             }
-            sKey[i] = key;
-        }
-        __syncthreads();
-        for (int k = 2; k <= N; k <<= 1) {  // bitonic sort in shared memory
-            for (int jj = k >> 1; jj > 0; jj >>= 1) {
-                for (int i = threadIdx.x; i < N; i += kThreads) {
-                    const int ixj = i ^ jj;
-                    if (ixj > i) {
-                        const int a = sKey[i], b = sKey[ixj];
-                        if ((a > b) == ((i & k) == 0)) {
-                            sKey[i] = b;
-                            sKey[ixj] = a;
-                        }
+            __syncthreads();
+            if (i < S) {
+                int rank = 0, pre = 0;
+                for (int j = 0; j < S; ++j) {
+                    const int kj = sKey[kTmp + j];
+                    if (kj < key) {
+                        ++rank;
+                        pre += 65535 - (kj >> 11);
                     }
                 }
-                __syncthreads();
+                sKey[rank] = key;
+                sP[rank] = pre;
+                if (rank == S - 1) sP[S] = pre + n;
             }
-        }
-        // exclusive prefix of the chunk counts in sorted order (contiguous runs per thread)
-        const int per = (S + kThreads - 1) / kThreads;
-        const int b0 = threadIdx.x * per;
-        const int b1 = min(S, b0 + per);
-        int mine = 0;
-        for (int i = b0; i < b1; ++i) mine += 65535 - (sKey[i] >> 11);
-        int incl = mine;  // inclusive scan over the warp, then over the warps
+        } else {
+            int N = 1;
+            while (N < S) N <<= 1;
+            for (int i = threadIdx.x; i < N; i += kThreads) {
+                int key = INT_MAX;
+                if (i < S) {
+                    const int L = clamp_len(p, p.seq_lens[i]);
+                    sL[i] = L;
+                    const int n = L > 0 ? (L + p.chunk - 1) / p.chunk : 1;
+                    key = ((65535 - n) << 11) | i;
+                }
+                sKey[i] = key;
+            }
+            __syncthreads();
+            for (int k = 2; k <= N; k <<= 1) {  // bitonic sort in shared memory
+                for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                    for (int i = threadIdx.x; i < N; i += kThreads) {
+                        const int ixj = i ^ jj;
+                        if (ixj > i) {
+                            const int a = sKey[i], b = sKey[ixj];
+                            if ((a > b) == ((i & k) == 0)) {
+                                sKey[i] = b;
+                                sKey[ixj] = a;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            // exclusive prefix of the chunk counts in sorted order (contiguous runs per thread)
+            const int per = (S + kThreads - 1) / kThreads;
+            const int b0 = threadIdx.x * per;
+            const int b1 = min(S, b0 + per);
+            int mine = 0;
+            for (int i = b0; i < b1; ++i) mine += 65535 - (sKey[i] >> 11);
+            int incl = mine;  // inclusive scan over the warp, then over the warps
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (lane == 31) warp_tot[warp] = incl;
+            __syncthreads();
+            int base = 0;
+            for (int w = 0; w < warp; ++w) base += warp_tot[w];
+            int run = base + incl - mine;
+            for (int i = b0; i < b1; ++i) {
+                sP[i] = run;
+                run += 65535 - (sKey[i] >> 11);
+            }
+            if (threadIdx.x == kThreads - 1) sP[S] = base + incl;
         }
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        int base = 0;
-        for (int w = 0; w < warp; ++w) base += warp_tot[w];
-        int run = base + incl - mine;
-        for (int i = b0; i < b1; ++i) {
-            sP[i] = run;
-            run += 65535 - (sKey[i] >> 11);
-        }
-        if (threadIdx.x == kThreads - 1) sP[S] = base + incl;
         if (threadIdx.x == 0) *sDry = 0;
+        if (threadIdx.x < kDecWarps) reinterpret_cast<int*>(smem + C::kTeamOff + kDecWarps * 16)[threadIdx.x] = 0;
         __syncthreads();
     }
 
@@ -210,12 +256,27 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
     uint32_t uses = 0;  // sub-pages this warp has streamed (ring position)
 
     // Items in heaviest-first sequence order, then head group, then chunk: a sequence's
-    // chunks are taken together, so its merge can start early. Each warp's first item is its own index
-    // (nothing to claim); later ones come from a device-wide counter.
+    // chunks are taken together, so its merge can start early. Each team's first item is its
+    // own index (nothing to claim); later ones come from a device-wide counter.
     const int n_warps = static_cast<int>(gridDim.x) * kDecWarps;
     const long long n_items = static_cast<long long>(sP[p.num_seqs]) * p.HG;
+    // Team size T: with at most half as many items as warps, T warps of a block share an
+    // item (sub-pages dealt round-robin, partials combined in shared memory), so that a
+    // small batch's cache reads spread over more warps. Every block derives the same T.
+    int T = 1;
+    while (T * 2 <= C::kMaxTeam && n_items * (T * 2) <= n_warps) T *= 2;
+    const int team = warp / T;  // team within the block
+    const int tw = warp % T;    // rank in the team = column slice of the merge
+    const long long n_teams = static_cast<long long>(gridDim.x) * (kDecWarps / T);
+    long long* sTeamT = reinterpret_cast<long long*>(smem + C::kTeamOff);           // [team][2]
+    volatile int* sTeamAbort = reinterpret_cast<int*>(smem + C::kTeamOff + kDecWarps * 16);  // [team]
+    float2* sML = reinterpret_cast<float2*>(smem + C::kTeamOff + kDecWarps * 20);   // [warp][row]
+    auto team_sync = [&]() {
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(T * 32) : "memory");
+    };
     bool first = true;
     bool waited = false;
+    uint32_t iter = 0;  // items this team has taken (its claim slot parity)
     // Work written by the previous launch (outputs, this launch's workspace) is touched
     // only after it has completed; set-up and cache reads may overlap its tail.
     auto wait_prior = [&]() {
@@ -228,9 +289,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         // ---------------------------------------------------------------- next item
         long long t = 0;
         if (first) {
-            t = static_cast<long long>(blockIdx.x) * kDecWarps + warp;
+            t = static_cast<long long>(blockIdx.x) * (kDecWarps / T) + team;
             first = false;
-        } else {
+        } else if (T == 1) {
             // nothing to claim when the first items covered everything, or once another
             // warp of this block has found the counter exhausted
             int dry = 0;
@@ -241,9 +302,26 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
             if (lane == 0) t = n_warps + static_cast<long long>(atomicAdd(p.work, 1ull));
             t = __shfl_sync(0xffffffffu, t, 0);
             if (t >= n_items && lane == 0) *sDry = 1;
+        } else {
+            if (n_items <= n_teams) break;  // the first items covered everything
+            wait_prior();
+            // the leader claims; the team reads the claim after the barrier (two slots by
+            // parity, so a slot is rewritten only after every member has read it)
+            if (tw == 0 && lane == 0) {
+                long long c = n_items;
+                if (!*sDry) {
+                    c = n_teams + static_cast<long long>(atomicAdd(p.work, 1ull));
+                    if (c >= n_items) *sDry = 1;
+                }
+                sTeamT[team * 2 + (iter & 1)] = c;
+            }
+            team_sync();
+            t = sTeamT[team * 2 + (iter & 1)];
         }
+        ++iter;
         if (t >= n_items) break;
-        const int qi = static_cast<int>(t / p.HG);  // in chunk units: sP[pos] <= qi < sP[pos + 1]
+        // in chunk units: sP[pos] <= qi < sP[pos + 1] (32-bit division when the items allow)
+        const int qi = n_items <= INT_MAX ? static_cast<int>(t) / p.HG : static_cast<int>(t / p.HG);
         int pos = 0;                                 // place in the heaviest-first order
         {
             int lo = 0, hi = p.num_seqs - 1;
@@ -258,20 +336,22 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         const int n_chunks = sP[pos + 1] - sP[pos];
         const int rem = static_cast<int>(t - static_cast<long long>(sP[pos]) * p.HG);
         const int hg = rem / n_chunks;
-        const int split = rem % n_chunks;
+        const int split = rem - hg * n_chunks;
         const int L = sL[seq];
-        const int hkv = hg / p.n_hgroups;
-        const int grp = hg % p.n_hgroups;
+        const int hkv = p.n_hgroups == 1 ? hg : hg / p.n_hgroups;
+        const int grp = hg - hkv * p.n_hgroups;
         const int hq0 = hkv * p.G + grp * kRowsPerItem;
         const int nvalid = min(kRowsPerItem, p.G - grp * kRowsPerItem);
         const size_t out_row0 = static_cast<size_t>(seq) * p.Hq + hq0;
 
         if (L == 0) {
-            // an empty sequence: O = 0, lse = -inf
+            // an empty sequence: O = 0, lse = -inf (written by the team's first warp)
             wait_prior();
-            for (int idx = lane; idx < nvalid * D; idx += 32)
-                p.o[out_row0 * D + idx] = __float2bfloat16_rn(0.0f);
-            if (lane < nvalid) p.lse[out_row0 + lane] = -INFINITY;
+            if (tw == 0) {
+                for (int idx = lane; idx < nvalid * D; idx += 32)
+                    p.o[out_row0 * D + idx] = __float2bfloat16_rn(0.0f);
+                if (lane < nvalid) p.lse[out_row0 + lane] = -INFINITY;
+            }
             continue;
         }
         const int tok0 = split * p.chunk;
@@ -279,6 +359,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         const int n_sub = (tok1 - tok0 + kSub - 1) / kSub;
         const int lb0 = tok0 / p.block_size;
         const int n_lb = (tok1 - 1) / p.block_size - lb0 + 1;
+        // this warp's sub-pages: tw, tw + T, tw + 2T, ... (none when n_sub <= tw)
+        const int n_mine = tw < n_sub ? (n_sub - tw + T - 1) / T : 0;
         int phys = 0;
         if (lane < n_lb) {
             phys = p.block_table[static_cast<size_t>(seq) * p.max_blocks + lb0 + lane];
@@ -296,23 +378,23 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
             const int ph = __shfl_sync(0xffffffffu, phys, lb - lb0);
             sub_row = (ph * p.Hkv + hkv) * p.block_size + (tok - lb * p.block_size);
         }
-        // Issue the TMA copies of sub-page i of this item into its ring stage: one copy for
-        // K and one for V, each landing as kBoxes 16-row boxes of 128 bytes.
-        auto issue = [&](int i) {
-            const int row = __shfl_sync(0xffffffffu, sub_row, i);
+        // Issue the TMA copies of this warp's k-th sub-page (item sub-page tw + k T) into
+        // its ring stage: one copy for K and one for V, each landing as kBoxes 16-row
+        // boxes of 128 bytes.
+        auto issue = [&](int k) {
+            const int row = __shfl_sync(0xffffffffu, sub_row, tw + k * T);
             if (lane == 0) {
-                const int s = static_cast<int>((uses + i) % C::kStages);
+                const int s = static_cast<int>((uses + k) % C::kStages);
                 const uint32_t dst = ring + s * C::kStageBytes;
                 mbar_arrive_expect_tx(full(s), C::kStageBytes);
                 tma_load_3d(dst, &tm_k, full(s), 0, row, 0);
                 tma_load_3d(dst + C::kSubBytes, &tm_v, full(s), 0, row, 0);
             }
         };
-        const int primed = min(C::kStages, n_sub);
-        for (int i = 0; i < primed; ++i) issue(i);
+        const int primed = min(C::kStages, n_mine);
+        for (int k = 0; k < primed; ++k) issue(k);
         int issued = primed;
         wait_prior();
-
         // q as A fragments (rows = query heads of this kv head, zero past nvalid)
         uint32_t qa[D / 16][4];
         {
@@ -333,12 +415,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.0f;
 
         bool ok = true;
-        for (int i = 0; i < n_sub; ++i) {
-            const int s = static_cast<int>((uses + i) % C::kStages);
-            if (!mbar_wait(full(s), ((uses + i) / C::kStages) & 1, nullptr, p.err)) {
+        for (int k = 0; k < n_mine; ++k) {
+            const int i = tw + k * T;  // sub-page of the item
+            const int s = static_cast<int>((uses + k) % C::kStages);
+            if (!mbar_wait(full(s), ((uses + k) / C::kStages) & 1, nullptr, p.err)) {
                 ok = false;
                 // never leave while a copy into this warp's ring is in flight
-                for (int j = i + 1; j < issued; ++j)
+                for (int j = k + 1; j < issued; ++j)
                     mbar_wait(full(static_cast<int>((uses + j) % C::kStages)), ((uses + j) / C::kStages) & 1,
                               nullptr, p.err);
                 break;
@@ -442,14 +525,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 mma_16816(o[2 * np + 1], pa, b2, b3);
             }
             __syncwarp();
-            if (i + C::kStages < n_sub) {
+            if (k + C::kStages < n_mine) {
                 // every read of the stage has returned (the P V products consumed them)
-                issue(i + C::kStages);
+                issue(k + C::kStages);
                 ++issued;
             }
         }
         uses += static_cast<uint32_t>(issued);
-        if (!ok) break;  // a copy timed out (reported): leave through the exit count
+        if (T == 1 && !ok) break;  // a copy timed out (reported): leave through the exit count
 
         // ---------------------------------------------------------------- item result
 #pragma unroll
@@ -458,7 +541,95 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
             l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
         }
         const int n_splits = (L + p.chunk - 1) / p.chunk;
-        if (n_splits == 1) {
+        // completion counter of this (sequence, head group) and column slice
+        const size_t done_idx = (static_cast<size_t>(seq) * p.HG + hg) * C::kMaxTeam + tw;
+        if (T > 1) {
+            // ---- team combine: each warp leaves its unnormalised O (rows x D, padded rows)
+            // in its own ring, idle now, and (m, l) per row; then warp tw combines columns
+            // [tw D/T, (tw + 1) D/T) of the team's T partials.
+            float* mine = reinterpret_cast<float*>(ring_ptr);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = g + 8 * h;
+                if (row >= nvalid) continue;
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt)
+                    *reinterpret_cast<float2*>(mine + row * C::kRowF + 8 * nt + 2 * tig) =
+                        make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+                if (tig == 0) sML[warp * kRowsPerItem + row] = make_float2(m[h], l[h]);
+            }
+            if (!ok && lane == 0) sTeamAbort[team] = 1;
+            fence_proxy_async_smem();  // these writes precede the ring's next TMA fills
+            team_sync();
+            if (sTeamAbort[team]) break;  // a member's copy timed out (reported): leave together
+            // lane r < nvalid: the weights 2^(m_w - M) of row r's members and 1 / L
+            float wt[C::kMaxTeam];
+            float inv_r = 0.0f;
+            {
+                const int r = lane < nvalid ? lane : 0;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < C::kMaxTeam; ++w)
+                    if (w < T) M = fmaxf(M, sML[(team * T + w) * kRowsPerItem + r].x);
+                float Ls = 0.0f;
+#pragma unroll
+                for (int w = 0; w < C::kMaxTeam; ++w) {
+                    wt[w] = 0.0f;
+                    if (w < T) {
+                        const float2 ml = sML[(team * T + w) * kRowsPerItem + r];
+                        wt[w] = ex2_approx(ml.x - M);  // 0 for a member with no sub-page
+                        Ls += wt[w] * ml.y;
+                    }
+                }
+                inv_r = 1.0f / Ls;
+                if (lane < nvalid) {
+                    if (n_splits == 1) {
+                        if (tw == 0) p.lse[out_row0 + r] = (M + log2f(Ls)) * kLn2;
+                    } else {
+                        // every member writes the row's log-sum (the same value): each column
+                        // slice's merge then reads one its own counter orders
+                        p.part_lse[(static_cast<size_t>(split) * p.num_seqs + seq) * p.Hq + hq0 + r] = M + log2f(Ls);
+                    }
+                }
+            }
+            const int cpl = D / 32 / T;   // columns per lane: 1, 2 or 4
+            const int c0 = tw * (D / T) + lane * cpl;
+            for (int r = 0; r < nvalid; ++r) {
+                float a[C::kMaxTeam];
+#pragma unroll
+                for (int w = 0; w < C::kMaxTeam; ++w) a[w] = __shfl_sync(0xffffffffu, wt[w], r);
+                const float inv = __shfl_sync(0xffffffffu, inv_r, r);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int w = 0; w < C::kMaxTeam; ++w) {
+                    if (w >= T) break;
+                    const float* src = reinterpret_cast<const float*>(smem + (team * T + w) * C::kWarpRingBytes) +
+                                       r * C::kRowF + c0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (j < cpl) acc[j] = fmaf(a[w], src[j], acc[j]);
+                }
+                if (n_splits == 1) {
+                    __nv_bfloat16* orow = p.o + (out_row0 + r) * D + c0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (j < cpl) orow[j] = __float2bfloat16_rn(acc[j] * inv);
+                } else {
+                    float* dst = p.part_o + ((static_cast<size_t>(split) * p.num_seqs + seq) * p.Hq + hq0 + r) * D + c0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (j < cpl) dst[j] = acc[j] * inv;
+                }
+            }
+            if (n_splits == 1) continue;
+            __threadfence();
+            __syncwarp();
+            int last_t = 0;
+            if (lane == 0) last_t = atomicAdd(p.done + done_idx, 1) == n_splits - 1;
+            last_t = __shfl_sync(0xffffffffu, last_t, 0);
+            if (!last_t) continue;
+        }
+        if (T == 1 && n_splits == 1) {
             // the whole sequence was this chunk: write O and lse directly
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -474,6 +645,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
             }
             continue;
         }
+        if (T == 1) {
         // several chunks: write this one's normalised partial and log-sum
         const size_t part_row0 = (static_cast<size_t>(split) * p.num_seqs + seq) * p.Hq + hq0;
 #pragma unroll
@@ -491,20 +663,24 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         __threadfence();
         __syncwarp();
         int last = 0;
-        if (lane == 0) last = atomicAdd(p.done + static_cast<size_t>(seq) * p.HG + hg, 1) == n_splits - 1;
+        if (lane == 0) last = atomicAdd(p.done + done_idx, 1) == n_splits - 1;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (!last) continue;
-        // ---- this warp finished the last chunk of (seq, head group): merge every partial.
-        // Eight lanes per query head (four heads at a time), each lane owning D/8
-        // consecutive columns. The chunks' log-sums are spread over a head's eight lanes
+        }
+        // ---- this warp finished the last chunk of (seq, head group) for its column slice
+        // (all D columns when T = 1): merge that slice of every partial. Eight lanes per
+        // query head (four heads at a time), each lane owning D/8/T consecutive columns.
+        // The chunks' log-sums are spread over a head's eight lanes
         // (chunk c on lane c % 8), kept in registers and reduced there; their weights reach
         // the other lanes by shuffle. The partial rows are read four chunks at a time with
         // independent 16-byte loads, the first four issued before the log-sums are reduced.
         __threadfence();
         {
-            constexpr int kCols = D / 8;           // columns per lane (16 or 8)
-            constexpr int kVec = kCols / 4;        // float4 loads per lane per chunk
+            constexpr int kCols = D / 8;           // columns per lane at most (16 or 8)
+            constexpr int kVec = kCols / 4;        // float4 loads per lane per chunk at most
             constexpr int kHeld = 8;               // log-sums per lane: up to 64 chunks in registers
+            const int cols = kCols / T;            // this slice's columns per lane (>= 4)
+            const int vec = cols / 4;
             const int slot_row = lane >> 3;        // head within the group of four
             const int cg = lane & 7;               // column group (and chunk c = cg mod 8)
             const size_t split_stride = static_cast<size_t>(p.num_seqs) * p.Hq;  // rows per chunk
@@ -513,13 +689,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 const bool live = row < nvalid;
                 const size_t r0 = static_cast<size_t>(seq) * p.Hq + hq0 + (live ? row : nvalid - 1);
                 const float* lse_r = p.part_lse + r0;
-                const float* po = p.part_o + r0 * D + cg * kCols;
+                const int col0 = tw * (D / T) + cg * cols;
+                const float* po = p.part_o + r0 * D + col0;
                 float acc[kCols];
 #pragma unroll
                 for (int t = 0; t < kCols; ++t) acc[t] = 0.0f;
                 auto add4 = [&](const float4 (&v)[kVec], float w) {
 #pragma unroll
                     for (int x = 0; x < kVec; ++x) {
+                        if (x >= vec) break;
                         acc[4 * x + 0] = fmaf(w, v[x].x, acc[4 * x + 0]);
                         acc[4 * x + 1] = fmaf(w, v[x].y, acc[4 * x + 1]);
                         acc[4 * x + 2] = fmaf(w, v[x].z, acc[4 * x + 2]);
@@ -528,16 +706,52 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 };
                 float M = -INFINITY, S = 0.0f;
                 if (n_splits <= 8 * kHeld) {
-                    // first four chunks' rows (n_splits >= 2), then the log-sums, all in flight
-                    const int c0n = min(4, n_splits);
-                    float4 v0[4][kVec];
+                    // A group of chunks' rows is loaded at once into v[4][kVec]: four chunks,
+                    // or eight when this slice's columns fill at most half a register row
+                    // (chunk c + 4 + k in the upper half). The first group is issued before
+                    // the log-sums are reduced.
+                    const bool wide = 2 * vec <= kVec;
+                    const int gsize = wide ? 8 : 4;
+                    auto load_group = [&](float4 (&v)[4][kVec], int c) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
+                        for (int k = 0; k < 4; ++k)
 #pragma unroll
-                        for (int x = 0; x < kVec; ++x)
-                            v0[k][x] = k < c0n ? __ldcg(reinterpret_cast<const float4*>(po + k * split_stride * D) + x)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int x = 0; x < kVec; ++x) {
+                                const bool up = wide && x >= kVec / 2;
+                                const int ch = c + k + (up ? 4 : 0);
+                                const int xx = up ? x - kVec / 2 : x;
+                                v[k][x] = (ch < n_splits && xx < vec)
+                                    ? __ldcg(reinterpret_cast<const float4*>(po + ch * split_stride * D) + xx)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                    };
                     float hl[kHeld];
+                    // weights of chunks c .. c + gsize - 1 come from register hl[c / 8] of lanes
+                    // 8 slot_row + (c % 8) ...
+                    const int src0 = slot_row * 8;
+                    auto add_group = [&](const float4 (&v)[4][kVec], int c, float hreg) {
+                        if (wide) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float w_lo = __shfl_sync(0xffffffffu, hreg, src0 + (c & 7) + k);
+                                const float w_hi = __shfl_sync(0xffffffffu, hreg, src0 + (c & 7) + 4 + k);
+#pragma unroll
+                                for (int x = 0; x < kVec / 2; ++x) {
+                                    if (x >= vec) break;
+                                    const float4 lo = v[k][x], hi = v[k][kVec / 2 + x];
+                                    acc[4 * x + 0] = fmaf(w_hi, hi.x, fmaf(w_lo, lo.x, acc[4 * x + 0]));
+                                    acc[4 * x + 1] = fmaf(w_hi, hi.y, fmaf(w_lo, lo.y, acc[4 * x + 1]));
+                                    acc[4 * x + 2] = fmaf(w_hi, hi.z, fmaf(w_lo, lo.z, acc[4 * x + 2]));
+                                    acc[4 * x + 3] = fmaf(w_hi, hi.w, fmaf(w_lo, lo.w, acc[4 * x + 3]));
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) add4(v[k], __shfl_sync(0xffffffffu, hreg, src0 + (c & 7) + k));
+                        }
+                    };
+                    float4 v0[4][kVec];
+                    load_group(v0, 0);
 #pragma unroll
                     for (int k = 0; k < kHeld; ++k) {
                         const int c = cg + 8 * k;
@@ -556,29 +770,19 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                     S += __shfl_xor_sync(0xffffffffu, S, 1);
                     S += __shfl_xor_sync(0xffffffffu, S, 2);
                     S += __shfl_xor_sync(0xffffffffu, S, 4);
-                    const int src0 = slot_row * 8;  // the lane holding chunk 8k + 0 of this head
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) add4(v0[k], __shfl_sync(0xffffffffu, hl[0], src0 + k));
+                    add_group(v0, 0, hl[0]);
 #pragma unroll
                     for (int kb = 0; kb < kHeld; ++kb) {
-                        // chunks 8 kb .. 8 kb + 7, four at a time (0..3 of kb = 0 are done)
+                        // chunks 8 kb .. 8 kb + 7: one group of eight or two of four
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
                             const int c = 8 * kb + 4 * half;
-                            if (c == 0) continue;
+                            if (c < gsize) continue;  // in the first group
                             if (c >= n_splits) break;
-                            const int cn = min(4, n_splits - c);
+                            if (wide && half == 1) break;  // covered by the group at 8 kb
                             float4 v[4][kVec];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                                for (int x = 0; x < kVec; ++x)
-                                    v[k][x] = k < cn
-                                        ? __ldcg(reinterpret_cast<const float4*>(po + (c + k) * split_stride * D) + x)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                add4(v[k], __shfl_sync(0xffffffffu, hl[kb], src0 + 4 * half + k));
+                            load_group(v, c);
+                            add_group(v, c, hl[kb]);
                         }
                     }
                 } else {
@@ -600,7 +804,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                             lv[k] = k < cn ? __ldcg(lse_r + (c + k) * split_stride) : -INFINITY;
 #pragma unroll
                             for (int x = 0; x < kVec; ++x)
-                                v[k][x] = k < cn
+                                v[k][x] = (k < cn && x < vec)
                                     ? __ldcg(reinterpret_cast<const float4*>(po + (c + k) * split_stride * D) + x)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
@@ -610,18 +814,25 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
                 }
                 if (live) {
                     const float inv = 1.0f / S;
-                    uint4* orow = reinterpret_cast<uint4*>(p.o + r0 * D + cg * kCols);
+                    __nv_bfloat16* ob = p.o + r0 * D + col0;
+                    if (cols >= 8) {
+                        uint4* orow = reinterpret_cast<uint4*>(ob);
 #pragma unroll
-                    for (int x = 0; x < kCols / 8; ++x)
-                        orow[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv, acc[8 * x + 1] * inv),
-                                             pack_bf16x2(acc[8 * x + 2] * inv, acc[8 * x + 3] * inv),
-                                             pack_bf16x2(acc[8 * x + 4] * inv, acc[8 * x + 5] * inv),
-                                             pack_bf16x2(acc[8 * x + 6] * inv, acc[8 * x + 7] * inv));
-                    if (cg == 0) p.lse[r0] = (M + log2f(S)) * kLn2;
+                        for (int x = 0; x < kCols / 8; ++x)
+                            if (8 * x < cols)
+                                orow[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv, acc[8 * x + 1] * inv),
+                                                     pack_bf16x2(acc[8 * x + 2] * inv, acc[8 * x + 3] * inv),
+                                                     pack_bf16x2(acc[8 * x + 4] * inv, acc[8 * x + 5] * inv),
+                                                     pack_bf16x2(acc[8 * x + 6] * inv, acc[8 * x + 7] * inv));
+                    } else {
+                        *reinterpret_cast<uint2*>(ob) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                                   pack_bf16x2(acc[2] * inv, acc[3] * inv));
+                    }
+                    if (tw == 0 && cg == 0) p.lse[r0] = (M + log2f(S)) * kLn2;
                 }
             }
         }
-        if (lane == 0) p.done[static_cast<size_t>(seq) * p.HG + hg] = 0;  // the last to touch it
+        if (lane == 0) p.done[done_idx] = 0;  // the last to touch it
     }
     // ---- leave: the last block of the grid puts the claim counters back to zero, so the
     // next launch on this workspace needs no memset (the completion counters were reset
@@ -695,9 +906,9 @@ int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, con
         prm.o = static_cast<__nv_bfloat16*>(o) + static_cast<size_t>(s0) * Hq * D;
         prm.lse = lse + static_cast<size_t>(s0) * Hq;
         prm.num_seqs = S;
-        // at most one item per warp beyond what the batch can hold
+        // at most one warp per item and team member beyond what the batch can hold
         const long long max_items =
-            static_cast<long long>(plan.n_split_max > 0 ? plan.n_split_max : 1) * S * prm.HG;
+            static_cast<long long>(plan.n_split_max > 0 ? plan.n_split_max : 1) * S * prm.HG * C::kMaxTeam;
         long long grid = sms;
         if (grid * kDecWarps > max_items) grid = (max_items + kDecWarps - 1) / kDecWarps;
         cudaLaunchConfig_t cfg = {};
@@ -743,7 +954,8 @@ bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_b
     if (n_split > 65535) return false;
     plan->chunk = chunk;
     plan->n_split_max = static_cast<int>(n_split);
-    plan->counters_bytes = ((16 + 4 * static_cast<size_t>(num_seqs) * hg + 255) / 256) * 256;
+    // one completion counter per (sequence, head group, merge column slice of a team)
+    plan->counters_bytes = ((16 + 4 * static_cast<size_t>(num_seqs) * hg * kMaxTeamAll + 255) / 256) * 256;
     const size_t rows = static_cast<size_t>(n_split) * num_seqs * Hq;
     plan->lse_offset = plan->counters_bytes;
     plan->o_offset = plan->lse_offset + ((rows * 4 + 255) / 256) * 256;

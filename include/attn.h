@@ -211,7 +211,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  *
  *   AK FlashDecoding: each chunk of a sequence's keys produces a partial output with
  *   its own max and sum; the partials are merged afterwards. The workspace holds
- *   those partials (fp32) for the largest possible split count of the batch.
+ *   the work counters (four completion counters per sequence and kv head group, one
+ *   per column slice a team of warps merges) and those partials (fp32) for the largest
+ *   possible split count of the batch.
  *   Returns 0 for invalid sizes.
  */
 size_t attn_decode_workspace_size(int num_seqs, int Hq, int Hkv, int d, int block_size,

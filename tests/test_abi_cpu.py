@@ -247,14 +247,15 @@ def test_decode_graph_argument_validation(lib):
 
 
 def test_workspace_size_matches_split_plan(lib):
-    """Counters (8-byte claim counter, 4-byte exit counter + pad, one int per (sequence, kv head)), then the fp32
-    partial log-sums and partial outputs of every possible split, 256-byte aligned."""
+    """Counters (8-byte claim counter, 4-byte exit counter + pad, four ints per (sequence, kv head): one per
+    column slice a team of up to four warps merges), then the fp32 partial log-sums and partial outputs of
+    every possible split, 256-byte aligned."""
     S, Hq, Hkv, d, bs, mb = 64, 32, 8, 128, 16, 2048
     chunk = eta.attn_decode_chunk_tokens(S, Hq, Hkv, bs, mb)
     n_split = -(-mb * bs // chunk)
     rows = n_split * S * Hq
     up = lambda x: -(-x // 256) * 256
-    want = up(16 + 4 * S * Hkv) + up(rows * 4) + rows * d * 4
+    want = up(16 + 4 * S * Hkv * 4) + up(rows * 4) + rows * d * 4
     assert eta.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb) == want
     assert eta.attn_decode_workspace_size(S, Hq, Hkv, 96, bs, mb) == 0
     assert chunk % bs == 0 and chunk % 16 == 0
@@ -280,7 +281,7 @@ def test_split_plan_halves_chunk_for_small_batches(lib):
     S, Hq, Hkv, d, bs, mb = 8, 32, 8, 128, 16, 125
     rows = (mb * bs // 128 + (mb * bs % 128 > 0)) * S * Hq
     up = lambda x: -(-x // 256) * 256
-    assert eta.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb) == up(16 + 4 * S * Hkv) + up(rows * 4) + rows * d * 4
+    assert eta.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb) == up(16 + 4 * S * Hkv * 4) + up(rows * 4) + rows * d * 4
 
 
 def test_split_plan_reproduces_flashdecoding_example(lib):

@@ -187,3 +187,48 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     eta.attn_fwd(q, k, v, causal=True)
     torch.cuda.synchronize()
     assert eta.attn_get_device_error() == 0
+
+
+def team_size(S, Hq, Hkv, d, bs, lens):
+    """The warps per item the kernel picks: the largest power of two up to d/32 with items x T
+    <= worker warps (152 x 8 on a full GB300), counted from the true lengths."""
+    mb = max(1, -(-max(lens) // bs))  # the generator's table width
+    chunk = eta.attn_decode_chunk_tokens(S, Hq, Hkv, bs, mb)
+    HG = Hkv * -(-(Hq // Hkv) // 16)
+    items = sum(max(1, -(-L // chunk)) for L in lens) * HG
+    n_split_max = -(-(mb * bs) // chunk)
+    kmax = d // 32
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    warps = min(sms, -(-(n_split_max * S * HG * kmax) // 8)) * 8
+    T = 1
+    while T * 2 <= kmax and items * T * 2 <= warps:
+        T *= 2
+    return T, chunk, items
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,d,lens,want_T", [
+    (3, 8, 2, 128, [1500, 700, 2000], 4),                  # few items: four warps per item
+    (8, 64, 8, 128, [600, 610, 590, 620, 605, 598, 615, 601], 2),
+    (8, 64, 8, 128, [1500, 1490, 1510, 1480, 1520, 1500, 1470, 1530], 1),
+    (3, 8, 2, 64, [1500, 700, 2000], 2),                    # d = 64: two warps at most
+    (16, 16, 8, 64, [3000 + 37 * i for i in range(16)], 1),
+    (1, 8, 2, 128, [9000], 4),                              # 71 chunks: the merge's long path
+    (5, 8, 2, 128, [0, 1, 5, 17, 33], 4),                   # fewer sub-pages than warps per item
+    (3, 64, 2, 128, [700, 1300, 90], 4),                    # 32 query heads per kv head: 2 groups
+])
+def test_warp_teams(oracle, S, Hq, Hkv, d, lens, want_T):
+    """Items shared by T warps of a block (sub-pages dealt round-robin, partials combined in
+    shared memory, the merge split into T column slices) against the oracle, for each T the
+    kernel can pick."""
+    T, chunk, items = team_size(S, Hq, Hkv, d, 16, lens)
+    assert T == want_T, (T, chunk, items)
+    case(oracle, S, Hq, Hkv, d, 16, lens=lens, seed=S + Hq + d, what=f"T={T} chunk={chunk} items={items}")
+
+
+@pytest.mark.parametrize("S", [255, 256, 257])
+def test_plan_order_paths(oracle, S):
+    """Up to 256 sequences the block orders them by counting, above by a bitonic sort: both
+    give the same work plan, so the results agree with the oracle on either side."""
+    r = np.random.default_rng(S)
+    lens = [int(v) for v in r.integers(0, 300, S)]
+    case(oracle, S, 8, 2, 128, 16, lens=lens, seed=S, what=f"S={S}")
