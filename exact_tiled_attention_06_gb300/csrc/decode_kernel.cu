@@ -670,10 +670,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         // ---- this warp finished the last chunk of (seq, head group) for its column slice
         // (all D columns when T = 1): merge that slice of every partial. Eight lanes per
         // query head (four heads at a time), each lane owning D/8/T consecutive columns.
-        // The chunks' log-sums are spread over a head's eight lanes
-        // (chunk c on lane c % 8), kept in registers and reduced there; their weights reach
-        // the other lanes by shuffle. The partial rows are read four chunks at a time with
-        // independent 16-byte loads, the first four issued before the log-sums are reduced.
+        // The chunks' log-sums are spread over a head's eight lanes (chunk c on lane c % 8),
+        // kept in registers and reduced there; their weights reach the other lanes by
+        // shuffle. The partial rows are read in groups of four chunks (eight when the
+        // slice is narrow) with independent 16-byte loads, the first group issued before
+        // the log-sums are reduced.
         __threadfence();
         {
             constexpr int kCols = D / 8;           // columns per lane at most (16 or 8)
