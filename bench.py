@@ -156,6 +156,7 @@ KERNEL_SOURCES = {
     "attn_fwd_sm103_paged": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_fwd_sm103_sparse": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_fwd_sm103_fp8": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_decode_sm103_c8_step": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
 }
 
 
@@ -694,7 +695,8 @@ def run_ours(args, rank, world, local_rank):
             "roofline": {"kernel": "attn_decode_sm103<128> (x n_layers, one graph)", "bound": "hbm",
                          "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} HBM copy",
-                         "traffic": None, "ms_per_step": round(graph_mean, 4),
+                         "traffic": load_traffic("attn_decode_sm103_c8_step"), "traffic_unit": "bytes per step",
+                         "ms_per_step": round(graph_mean, 4),
                          "ms_p10_p50_p90": [round(float(np.percentile(graph_ms, x)), 4) for x in (10, 50, 90)]},
         }
     return result
