@@ -80,13 +80,14 @@ ATTN_API int attn_decode_graph_create(int n_layers, const void* const* q, const 
         cudaStreamDestroy(s);
         return kErrCuda;
     }
-    // Layer 0 zeroes the counters; every launch leaves them at zero, so the later layers
-    // skip the memset and launch as programmatic dependents of the layer before: their
-    // set-up and first cache reads overlap its tail.
+    // Layer 0 zeroes the counters; each launch zeroes the claim counter the next one uses
+    // (the two alternate), so the later layers skip the memset and launch as programmatic
+    // dependents of the layer before: their set-up and first cache reads overlap its tail.
+    int slot = 0;
     for (int l = 0; l < n_layers && rc == kOk; ++l)
         rc = launch_decode(q[l], k_cache[l], v_cache[l], block_table, seq_lens, o[l], lse[l], num_seqs, Hq, Hkv, d,
                            block_size, max_blocks_per_seq, num_blocks, scale, workspace, plan, s, err,
-                           l == 0 ? 0 : (kDecodeCountersZeroed | kDecodeChained));
+                           l == 0 ? 0 : (kDecodeCountersZeroed | kDecodeChained), &slot);
     cudaGraph_t graph = nullptr;
     const cudaError_t end = cudaStreamEndCapture(s, &graph);
     cudaStreamDestroy(s);

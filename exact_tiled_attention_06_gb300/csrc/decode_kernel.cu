@@ -23,11 +23,12 @@
 //     last chunk of a (sequence, head group) -- per column slice for a team -- merges
 //     all its partials and writes O and lse. A sequence that fits in one chunk is
 //     written directly.
-// Every launch leaves its counters at zero (the merging warp resets its completion
-// counter, the last warp to leave resets the claim counters), and every block signals
-// programmatic dependents at its start and waits for its own predecessor before touching
-// outputs or workspace, so a chain of decode launches (the layers of a captured step)
-// needs one memset and overlaps each launch's set-up with the previous one's tail.
+// A launch leaves its completion counters at zero (each is reset by the warp that merges)
+// and claims from one of two counters, zeroing the other for the next launch of a chain;
+// every block signals programmatic dependents at its start and waits for its own
+// predecessor before touching outputs or workspace, so a chain of decode launches (the
+// layers of a captured step) needs one memset, no block waits at its exit, and each
+// launch's set-up overlaps the previous one's tail.
 //
 // Pages: "Modern attention kernels", "Prefill and decode need different kernels"
 // (decode is memory-bound: wide contiguous cache reads, one query's context spread over
@@ -96,8 +97,8 @@ struct DecParams {
     const int32_t* seq_lens;
     __nv_bfloat16* o;
     float* lse;
-    unsigned long long* work;  // dynamic items claimed after each warp's first
-    unsigned* exits;           // blocks that have left the work loop
+    unsigned long long* work;       // dynamic items claimed after each team's first
+    unsigned long long* work_next;  // the claim counter of the next launch of a chain
     int* done;                 // [num_seqs][HG] chunks finished
     float* part_o;             // [n_split_max][num_seqs][Hq][D]
     float* part_lse;           // [n_split_max][num_seqs][Hq], log2 units
@@ -835,19 +836,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         }
         if (lane == 0) p.done[done_idx] = 0;  // the last to touch it
     }
-    // ---- leave: the last block of the grid puts the claim counters back to zero, so the
-    // next launch on this workspace needs no memset (the completion counters were reset
-    // by the warps that merged). Every warp of the block has stopped claiming here.
+    // ---- leave. The next launch of a chain claims from the other counter, last used by
+    // this launch's predecessor, which has completed once wait_prior returns: block 0
+    // zeroes it, so the chain needs one memset and no block waits at its exit (the
+    // completion counters were reset by the warps that merged). The wait also keeps this
+    // launch from completing before its predecessor.
     wait_prior();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(p.exits, 1u) == gridDim.x - 1) {
-            *p.work = 0ull;
-            *p.exits = 0u;
-            __threadfence();
-        }
-    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.work_next = 0ull;
 }
 
 
@@ -855,12 +850,13 @@ template <int D>
 int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                     const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int block_size,
                     int max_blocks, int num_blocks, float scale, void* workspace, const DecodePlan& plan,
-                    cudaStream_t stream, unsigned* err, int flags)
+                    cudaStream_t stream, unsigned* err, int flags, int* chain_slot)
 {
     using C = DecCfg<D>;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    // the claim counters and the completion counters must start at zero; every launch
-    // leaves them at zero again, so a chain of launches needs this only once
+    // the claim counters and the completion counters must start at zero; a launch leaves
+    // its completion counters at zero and zeroes the next launch's claim counter, so a
+    // chain of launches needs this only once
     if (!(flags & kDecodeCountersZeroed) && cudaMemsetAsync(ws, 0, plan.counters_bytes, stream) != cudaSuccess)
         return kErrCuda;
     // The cache as rows of D elements, each row seen as kBoxes 64-column pieces: dims
@@ -881,8 +877,7 @@ int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, con
         cudaSuccess)
         return kErrCuda;
     DecParams prm;
-    prm.work = reinterpret_cast<unsigned long long*>(ws);
-    prm.exits = reinterpret_cast<unsigned*>(ws + 8);
+    int slot = chain_slot ? (*chain_slot & 1) : 0;  // claim counters at ws and ws + 8
     prm.done = reinterpret_cast<int*>(ws + 16);
     prm.part_lse = reinterpret_cast<float*>(ws + plan.lse_offset);
     prm.part_o = reinterpret_cast<float*>(ws + plan.o_offset);
@@ -923,8 +918,12 @@ int launch_decode_d(const void* q, const void* k_cache, const void* v_cache, con
         const bool chained = (flags & kDecodeChained) || s0 > 0;
         cfg.attrs = chained ? attr : nullptr;
         cfg.numAttrs = chained ? 1 : 0;
+        prm.work = reinterpret_cast<unsigned long long*>(ws + 8 * slot);
+        prm.work_next = reinterpret_cast<unsigned long long*>(ws + 8 * (slot ^ 1));
         if (cudaLaunchKernelEx(&cfg, attn_decode_sm103<D>, tk, tv, prm) != cudaSuccess) return kErrLaunch;
+        slot ^= 1;
     }
+    if (chain_slot) *chain_slot = slot;
     return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 
@@ -967,14 +966,16 @@ bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_b
 int launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                   const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size,
                   int max_blocks_per_seq, int num_blocks, float scale, void* workspace, const DecodePlan& plan,
-                  cudaStream_t stream, unsigned* err, int flags)
+                  cudaStream_t stream, unsigned* err, int flags, int* chain_slot)
 {
     if (d == 128)
         return launch_decode_d<128>(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, block_size,
-                                    max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err, flags);
+                                    max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err, flags,
+                                   chain_slot);
     if (d == 64)
         return launch_decode_d<64>(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, block_size,
-                                   max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err, flags);
+                                   max_blocks_per_seq, num_blocks, scale, workspace, plan, stream, err, flags,
+                                   chain_slot);
     return kErrUnsupported;
 }
 

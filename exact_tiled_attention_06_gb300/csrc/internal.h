@@ -80,9 +80,12 @@ struct DecodePlan {
 bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
                  DecodePlan* plan);
 
-// Decode (implemented in decode_kernel.cu). Arguments are already validated. flags:
+// Decode (implemented in decode_kernel.cu). Arguments are already validated. A launch
+// claims work from one of the workspace's two claim counters, and zeroes the other for
+// the next launch of a chain once its own predecessor has completed. chain_slot (may be
+// null: slot 0) holds the first launch's counter and receives the next launch's. flags:
 //   kDecodeCountersZeroed -- the workspace's counters are known to be zero (the previous
-//                            launch on it completed normally): no memset is enqueued;
+//                            launch of the chain completed normally): no memset is enqueued;
 //   kDecodeChained        -- launch as a programmatic dependent of the previous launch on
 //                            the stream (its set-up and cache reads overlap that launch's
 //                            tail; everything else waits for it to complete).
@@ -91,7 +94,8 @@ constexpr int kDecodeChained = 2;
 int launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                   const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
                   int block_size, int max_blocks_per_seq, int num_blocks, float scale, void* workspace,
-                  const DecodePlan& plan, cudaStream_t stream, unsigned* err, int flags);
+                  const DecodePlan& plan, cudaStream_t stream, unsigned* err, int flags,
+                  int* chain_slot = nullptr);
 
 // Backward workspace: D_i [B][Hq][Nq] fp32 at dvec_offset, then the fp32 dQ accumulator
 // [B][Hq][Nq][d] at dq_offset (256-byte aligned).

@@ -299,8 +299,9 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
  *     per sequence; each layer has its own cache). The layers run in order, one after
  *     another, so one workspace of attn_decode_workspace_size(...) bytes serves them all.
  *     Captures, on a private stream, one counter memset and then each layer's decode
- *     kernel(s); every decode launch leaves the counters at zero, so layers after the
- *     first need no memset and are launched as programmatic dependents of the layer
+ *     kernel(s); a decode launch leaves its completion counters at zero and zeroes the
+ *     claim counter of the next launch (two alternate), so layers after the first need
+ *     no memset and are launched as programmatic dependents of the layer
  *     before (their set-up and first cache reads overlap its tail; everything they write
  *     waits for it to complete). Then instantiates the graph; nothing runs. On success
  *     *graph_out holds an opaque handle (host memory and CUDA graph objects owned by the

@@ -247,7 +247,7 @@ def test_decode_graph_argument_validation(lib):
 
 
 def test_workspace_size_matches_split_plan(lib):
-    """Counters (8-byte claim counter, 4-byte exit counter + pad, four ints per (sequence, kv head): one per
+    """Counters (two 8-byte claim counters, four ints per (sequence, kv head): one per
     column slice a team of up to four warps merges), then the fp32 partial log-sums and partial outputs of
     every possible split, 256-byte aligned."""
     S, Hq, Hkv, d, bs, mb = 64, 32, 8, 128, 16, 2048

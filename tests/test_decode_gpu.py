@@ -156,8 +156,9 @@ def test_more_sequences_than_one_launch_holds(oracle):
 
 
 def test_counters_left_at_zero_for_the_next_call():
-    """Every launch puts its counters back to zero: a workspace reused by back-to-back calls
-    of different batches gives the same results as fresh workspaces."""
+    """A launch puts its completion counters back to zero and zeroes the claim counter the
+    next launch of a chain uses: a workspace reused by back-to-back calls of different
+    batches gives the same results as fresh workspaces."""
     xa = inputs.decode_inputs(6, 8, 2, 128, 16, len_lo=1, len_hi=3000, seed=22)
     xb = inputs.decode_inputs(3, 8, 2, 128, 16, len_lo=1, len_hi=700, seed=23, max_blocks_per_seq=190)
     ws = torch.zeros(max(eta.attn_decode_workspace_size(6, 8, 2, 128, 16, xa.block_table.shape[1]),
@@ -169,9 +170,11 @@ def test_counters_left_at_zero_for_the_next_call():
         for x, ref in ((xa, ref_a), (xb, ref_b)):
             o, lse = run_decode(x, scale, workspace=ws)
             assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1])
-    n_ctr = 16 + 4 * 6 * 2  # claim counter, exit counter and pad, one completion counter per (seq, kv head)
+    # claim counters: the one the next launch would use is zero; completion counters: four
+    # per (sequence, kv head), all zero
     torch.cuda.synchronize()
-    assert int(ws[:n_ctr].count_nonzero()) == 0
+    assert int(ws[8:16].count_nonzero()) == 0
+    assert int(ws[16:16 + 4 * 6 * 2 * 4].count_nonzero()) == 0
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
