@@ -235,3 +235,25 @@ def test_plan_order_paths(oracle, S):
     r = np.random.default_rng(S)
     lens = [int(v) for v in r.integers(0, 300, S)]
     case(oracle, S, 8, 2, 128, 16, lens=lens, seed=S, what=f"S={S}")
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,d,lo,hi", [
+    (3, 8, 2, 128, 1, 2500),      # four warps per item
+    (8, 64, 8, 128, 590, 620),    # two warps per item
+    (3, 8, 2, 64, 1, 2500),       # d = 64, two warps per item
+    (16, 16, 8, 64, 2900, 3500),  # one warp per item
+    (300, 8, 2, 128, 0, 300),     # the bitonic-sort plan, empty sequences among them
+])
+def test_repeated_launches_are_bitwise_identical(S, Hq, Hkv, d, lo, hi):
+    """Claims, team combines and per-slice merges race for nothing: thirty launches on one
+    workspace give the same bits."""
+    x = inputs.decode_inputs(S, Hq, Hkv, d, 16, len_lo=lo, len_hi=hi, seed=S + d)
+    args = [t.cuda() for t in (x.q, x.k_cache, x.v_cache, x.block_table, x.seq_lens)]
+    ws = torch.empty(eta.attn_decode_workspace_size(S, Hq, Hkv, d, 16, x.block_table.shape[1]), dtype=torch.uint8,
+                     device="cuda")
+    o0, l0 = eta.attn_decode(*args, workspace=ws)
+    for _ in range(30):
+        o, lse = eta.attn_decode(*args, workspace=ws)
+        assert torch.equal(o, o0) and torch.equal(lse, l0)
+    torch.cuda.synchronize()
+    assert eta.attn_get_device_error() == 0
