@@ -75,3 +75,25 @@ def test_blocksparse_pairs():
     eye = np.eye(3, dtype=bool)
     assert bench.blocksparse_pairs(eye, 384, 384, False, -1) == 3 * 128 * 128
     assert bench.blocksparse_pairs(eye, 384, 384, True, -1) == 3 * 128 * 129 // 2
+
+
+def test_traffic_records_are_well_formed(monkeypatch):
+    """Every DRAM-traffic record names a kernel whose sources the bench hashes, and the bench
+    reports a record's bytes only while those sources are the ones it was captured on."""
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles",
+                        "dram_traffic.json")
+    with open(path) as f:
+        records = {k: v for k, v in json.load(f).items() if not k.startswith("_")}
+    assert records
+    for name, rec in records.items():
+        assert name in bench.KERNEL_SOURCES, name
+        assert isinstance(rec["bytes_per_launch"], int) and rec["bytes_per_launch"] > 0, name
+        assert len(rec["source_hash"]) == 16 and int(rec["source_hash"], 16) >= 0, name
+        assert rec["case"], name
+        monkeypatch.setattr(bench, "kernel_source_hash", lambda k, h=rec["source_hash"]: h)
+        assert bench.load_traffic(name) == float(rec["bytes_per_launch"])
+        monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
+        assert bench.load_traffic(name) is None
+    # decode: within a few percent of the algorithmic bytes it was captured against
+    assert 1.0 < records["attn_decode_sm103"]["bytes_per_launch"] / 3884961792 < 1.05
+    assert 1.0 < records["attn_decode_sm103_c8_step"]["bytes_per_launch"] / 1071251456 < 1.05
