@@ -72,7 +72,7 @@ def test_length_boundaries(oracle, d):
     case(oracle, len(LENS), 8, 2, d, 16, lens=LENS, seed=2, what=f"lengths d={d}")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (32, 8), (16, 2), (16, 1), (32, 1), (12, 4)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (32, 8), (16, 2), (16, 1), (32, 1), (12, 4), (12, 1), (48, 2)])
 def test_group_sizes(oracle, Hq, Hkv):
     case(oracle, 5, Hq, Hkv, 128, 16, lo=1, hi=1500, seed=Hq + Hkv, what=f"G={Hq // Hkv}")
 
