@@ -140,6 +140,31 @@ int encode_f32_map(CUtensorMap* map, const void* base, int rank, const uint64_t*
                       strides_bytes, box);
 }
 
+int validate_decode_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                         const int32_t* seq_lens, const void* o, const float* lse, int num_seqs, int Hq, int Hkv,
+                         int d, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                         DecodePlan* plan, bool* empty)
+{
+    *empty = false;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return kErrInvalidArg;
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || num_blocks <= 0) return kErrInvalidArg;
+    if (Hq % Hkv != 0) return kErrInvalidArg;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return kErrInvalidArg;
+    if (num_seqs > 65535) return kErrInvalidArg;
+    if (d != 64 && d != 128) return kErrUnsupported;
+    if (block_size < 16 || block_size > 256 || block_size % 16 != 0) return kErrUnsupported;
+    if (static_cast<long long>(num_blocks) * Hkv * block_size > INT32_MAX) return kErrUnsupported;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned4(lse) ||
+        !aligned4(block_table) || !aligned4(seq_lens))
+        return kErrMisaligned;
+    if (num_seqs == 0) {
+        *empty = true;
+        return kOk;
+    }
+    if (!decode_plan(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_seq, plan)) return kErrInvalidArg;
+    return kOk;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -317,25 +342,16 @@ ATTN_API int attn_decode(const void* q, const void* k_cache, const void* v_cache
                          size_t workspace_bytes, void* stream)
 {
     // ---- arguments (no CUDA call before these checks)
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return kErrInvalidArg;
-    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || num_blocks <= 0) return kErrInvalidArg;
-    if (Hq % Hkv != 0) return kErrInvalidArg;
-    if (!(scale > 0.0f) || !std::isfinite(scale)) return kErrInvalidArg;
-    if (num_seqs > 65535) return kErrInvalidArg;
-    if (d != 64 && d != 128) return kErrUnsupported;
-    if (block_size < 16 || block_size > 256 || block_size % 16 != 0) return kErrUnsupported;
-    if (static_cast<long long>(num_blocks) * Hkv * block_size > INT32_MAX) return kErrUnsupported;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned4(lse) ||
-        !aligned4(block_table) || !aligned4(seq_lens))
-        return kErrMisaligned;
-    if (num_seqs == 0) return kOk;
     DecodePlan plan;
-    if (!decode_plan(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_seq, &plan)) return kErrInvalidArg;
+    bool empty = false;
+    int rc = validate_decode_args(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, d,
+                                  block_size, max_blocks_per_seq, num_blocks, scale, &plan, &empty);
+    if (rc != kOk || empty) return rc;
     if (!workspace || workspace_bytes < plan.bytes) return kErrWorkspace;
     if (!aligned16(workspace)) return kErrMisaligned;
     // ---- device
     int dev = 0;
-    int rc = check_device(&dev);
+    rc = check_device(&dev);
     if (rc != kOk) return rc;
     unsigned* err = device_error_word();
     if (!err) return kErrCuda;

@@ -42,7 +42,6 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -980,86 +979,3 @@ int launch_decode(const void* q, const void* k_cache, const void* v_cache, const
 }
 
 }  // namespace attn
-
-// ============================================================================
-// attn_decode_noalloc: the decode above with its scratch in a static device array.
-//
-// Some callers cannot allocate device memory where they run decode: a serving
-// runtime that has reserved nearly all of HBM for its KV-cache pool and forbids any
-// further cudaMalloc, or a plugin that runs inside another framework's execution
-// plan, where allocation calls are not allowed. They cannot supply the workspace
-// attn_decode needs, so this entry point uses a fixed array that lives in the
-// library's module instead: every GPU that loads libattn.so holds these bytes until
-// the process exits. It allocates nothing (no cudaMalloc, cudaFree or allocating
-// library call); the caller still passes every input and output.
-// ============================================================================
-namespace attn {
-namespace {
-
-// Upper bound of the split-KV partials this entry point can hold (64 MiB).
-constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
-
-// The scratch itself. Host code must not pass this name to a kernel: on the host it
-// is only a stand-in for the symbol, not a device address.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// Device address of the scratch on the current device, looked up once per device.
-int noalloc_scratch(void** out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return kErrUnsupported;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return kErrCuda;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
-    return kOk;
-}
-
-}  // namespace
-}  // namespace attn
-
-extern "C" __attribute__((visibility("default"))) int attn_decode_noalloc(
-    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
-    void* o, float* lse, int num_seqs, int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
-    int num_blocks, float scale, void* stream)
-{
-    using namespace attn;
-    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return kErrInvalidArg;
-    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || num_blocks <= 0) return kErrInvalidArg;
-    if (Hq % Hkv != 0) return kErrInvalidArg;
-    if (!(scale > 0.0f) || !isfinite(scale)) return kErrInvalidArg;
-    if (num_seqs > 65535) return kErrInvalidArg;
-    if (d != 64 && d != 128) return kErrUnsupported;
-    if (block_size < 16 || block_size > 256 || block_size % 16 != 0) return kErrUnsupported;
-    if (static_cast<long long>(num_blocks) * Hkv * block_size > INT32_MAX) return kErrUnsupported;
-    if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(o) || !a4(lse) || !a4(block_table) || !a4(seq_lens))
-        return kErrMisaligned;
-    if (num_seqs == 0) return kOk;
-    DecodePlan plan;
-    if (!decode_plan(num_seqs, Hq, Hkv, d, block_size, max_blocks_per_seq, &plan)) return kErrInvalidArg;
-    if (plan.bytes > kNoAllocScratchBytes) return kErrWorkspace;  // sizes beyond the static scratch
-    int major = 0, minor = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return kErrCuda;
-    if (major != 10 || minor != 3) return kErrUnsupported;
-    void* scratch = nullptr;
-    int rc = noalloc_scratch(&scratch);
-    if (rc != kOk) return rc;
-    unsigned* err = device_error_word();
-    if (!err) return kErrCuda;
-    return launch_decode(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, Hq, Hkv, d, block_size,
-                         max_blocks_per_seq, num_blocks, scale, scratch, plan, static_cast<cudaStream_t>(stream),
-                         err, 0);
-}

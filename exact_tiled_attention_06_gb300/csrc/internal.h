@@ -91,6 +91,14 @@ bool decode_plan(int num_seqs, int Hq, int Hkv, int d, int block_size, int max_b
 //                            tail; everything else waits for it to complete).
 constexpr int kDecodeCountersZeroed = 1;
 constexpr int kDecodeChained = 2;
+// Host-side checks of attn_decode's arguments, shared by every decode entry point (no CUDA
+// call). On kOk, *plan holds the split plan and *empty is true when there is nothing to
+// compute (num_seqs == 0). The workspace is the caller's to check against plan->bytes.
+int validate_decode_args(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                         const int32_t* seq_lens, const void* o, const float* lse, int num_seqs, int Hq, int Hkv,
+                         int d, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                         DecodePlan* plan, bool* empty);
+
 int launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                   const int32_t* seq_lens, void* o, float* lse, int num_seqs, int Hq, int Hkv, int d,
                   int block_size, int max_blocks_per_seq, int num_blocks, float scale, void* workspace,

@@ -17,7 +17,9 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *    Every launch is asynchronous on that stream; the library never synchronises it.
  *  - The caller owns every buffer (inputs, outputs, workspace). The library never
- *    allocates or frees device memory.
+ *    allocates or frees device memory. The one fixed device allocation it carries is
+ *    attn_decode_noalloc's static 64 MiB scratch array, which sits in a module of its own:
+ *    a GPU holds it only after attn_decode_noalloc has been called on it.
  *  - Host-detectable problems return a negative attn_status before anything is
  *    launched. Problems the kernels detect (a block-table entry out of range, a
  *    pipeline wait that ran out of time) set a device error word that
@@ -266,17 +268,21 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *   nearly all of HBM for its KV-cache pool and forbids further cudaMalloc, or a
  *   plugin running inside another framework's execution plan, where allocation calls
  *   are not allowed). This variant keeps the split-KV partials in a static device
- *   array inside libattn.so instead: 64 MiB, held on every GPU that loads the library
- *   until the process exits. It allocates nothing; the caller still passes every input
- *   and output, with the same meaning, layout and alignment as attn_decode.
+ *   array inside libattn.so instead: 64 MiB, in a module that holds nothing else, so a
+ *   GPU holds it from the first attn_decode_noalloc call on that device (the runtime
+ *   loads the module then) until the process exits; processes that never call it never
+ *   hold it. It allocates nothing (no cudaMalloc, cudaFree or allocating library call);
+ *   the caller still passes every input and output, with the same meaning, layout and
+ *   alignment as attn_decode, and gets the same argument checks and statuses.
  *
  *   Returns ATTN_ERR_WORKSPACE when attn_decode_workspace_size(...) for these sizes
- *   exceeds 64 MiB. The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) and caches it; make that first call before any stream
- *   capture. Every call shares the one array, so calls that overlap on the GPU (on
- *   different streams, or from different threads) race and corrupt each other's
- *   results; serialise them. The array keeps the last call's contents, and nothing in
- *   it needs to start at zero: each call reads only partials it has written itself.
+ *   exceeds 64 MiB, before anything is launched. The first call on a device, with that
+ *   device current, looks up the array's device address (cudaGetSymbolAddress) and
+ *   caches it; make that first call before any stream capture. Every call shares the
+ *   one array, so calls that overlap on the GPU (on different streams, or from different
+ *   threads) race and corrupt each other's results; serialise them. The array keeps the
+ *   last call's contents: each call first zeroes the counters it needs on the stream
+ *   (one small cudaMemsetAsync), and reads only partials it has written itself.
  */
 int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_table, const int32_t* seq_lens, void* o, float* lse,

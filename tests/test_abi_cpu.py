@@ -210,6 +210,26 @@ def test_decode_argument_validation(lib):
     assert dec(lib, S=0) == 0                 # empty batch: no launch
 
 
+def test_noalloc_decode_validates_like_decode(lib):
+    """attn_decode_noalloc shares attn_decode's argument checks: the same bad arguments give
+    the same status, before any CUDA call (no GPU here)."""
+    cases = [dict(q=None), dict(bt=None), dict(Hq=6, Hkv=4), dict(nb=0), dict(scale=-1.0), dict(d=80), dict(bs=8),
+             dict(bs=24), dict(bs=512), dict(nb=1 << 26), dict(kc=FAKE + 4), dict(lse=FAKE + 2), dict(S=-1),
+             dict(S=70000), dict(mb=-1), dict(S=0)]
+    for kw in cases:
+        a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, o=FAKE, lse=FAKE, S=4, Hq=8, Hkv=2, d=128, bs=16, mb=64,
+                 nb=256, scale=0.1)
+        a.update(kw)
+        want = dec(lib, **kw)
+        got = lib.attn_decode_noalloc(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["o"], a["lse"], a["S"], a["Hq"],
+                                      a["Hkv"], a["d"], a["bs"], a["mb"], a["nb"], a["scale"], None)
+        assert got == want, (kw, got, want)
+    # partials beyond the 64 MiB static scratch: rejected before any CUDA call
+    assert lib.attn_decode_workspace_size(64, 32, 8, 128, 16, 2048) > 64 << 20
+    assert lib.attn_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 32, 8, 128, 16, 2048, 1000, 0.1,
+                                   None) == -4
+
+
 def graph_create(lib, n=2, bad_layer=None, field=None, value=None, S=4, Hq=8, Hkv=2, d=128, bs=16, mb=64, nb=256,
                  scale=0.1, ws=FAKE, ws_bytes=None, out_ptr=True):
     """attn_decode_graph_create with fake pointers; (field, value) replaces one pointer of

@@ -1,8 +1,13 @@
 """GPU: attn_decode_noalloc, the decode entry point for callers that cannot allocate
-device memory (a runtime that reserved HBM for its own pools, a plugin inside another
-framework's execution plan). Its split partials live in a static array inside the
-library. Called through the C ABI twice in a row, its output must match attn_decode
-(with a caller-supplied workspace) within the parity tolerances of the other tests.
+device memory where they run decode (a serving runtime that reserved HBM for its own
+pools and forbids further cudaMalloc, a plugin inside another framework's execution plan
+where allocation calls are not allowed). Its split partials live in a static array inside
+the library instead of a caller-supplied workspace.
+
+Called through the C ABI twice in a row (the shared array keeps the first call's
+contents), its output must match both the fp64 oracle and attn_decode with a caller-
+supplied workspace, within the tolerances of the other parity tests, and the device's
+free memory must not change between the two calls.
 
 This file is collected last on purpose, and it passes both alone and after the rest.
 """
@@ -13,6 +18,7 @@ import torch
 
 import exact_tiled_attention_06_gb300 as eta
 from exact_tiled_attention_06_gb300 import inputs
+from tests.gpu_util import check_attention, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -31,11 +37,12 @@ def _compare(o, lse, o_ref, lse_ref):
     assert rel.max().item() <= LSE_REL
 
 
-def test_noalloc_decode_matches_workspace_decode():
+@pytest.mark.parametrize("d", [64, 128])
+def test_noalloc_decode_matches_oracle_and_workspace_decode(oracle, d):
     eta.build()
     lib = eta.load_library()
-    S, Hq, Hkv, d, bs = 12, 32, 8, 128, 16
-    x = inputs.decode_inputs(S, Hq, Hkv, d, bs, len_lo=1, len_hi=6000, seed=21, extra_blocks=4, poison=True)
+    S, Hq, Hkv, bs = 12, 32, 8, 16
+    x = inputs.decode_inputs(S, Hq, Hkv, d, bs, len_lo=1, len_hi=6000, seed=21 + d, extra_blocks=4, poison=True)
     x.seq_lens[0] = 0  # an empty sequence too
     dev = torch.device("cuda")
     q, kc, vc = x.q.to(dev), x.k_cache.to(dev), x.v_cache.to(dev)
@@ -44,29 +51,50 @@ def test_noalloc_decode_matches_workspace_decode():
     scale = 1.0 / math.sqrt(d)
     assert eta.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb) <= 64 << 20
 
-    o_ref, lse_ref = eta.attn_decode(q, kc, vc, bt, sl, scale=scale)
+    o_ws, lse_ws = eta.attn_decode(q, kc, vc, bt, sl, scale=scale)
     torch.cuda.synchronize()
     assert eta.attn_get_device_error() == 0
+    kc64 = torch.nan_to_num(x.k_cache.double()).numpy()
+    vc64 = torch.nan_to_num(x.v_cache.double()).numpy()
+    o_ref, lse_ref = oracle.attn_decode(f64(x.q), kc64, vc64, x.block_table.numpy(), x.seq_lens.numpy(), scale)
 
+    # outputs for both calls exist before the first one, so nothing in between allocates
+    outs = [(torch.full_like(q, float("nan")), torch.full((S, Hq), float("nan"), dtype=torch.float32, device=dev))
+            for _ in range(2)]
     stream = torch.cuda.current_stream().cuda_stream or None
-    for _ in range(2):  # two calls in a row: the shared array keeps the previous call's contents
-        o = torch.full_like(q, float("nan"))
-        lse = torch.full((S, Hq), float("nan"), dtype=torch.float32, device=dev)
+    free = []
+    for o, lse in outs:  # two calls in a row: the shared array keeps the previous call's contents
         rc = lib.attn_decode_noalloc(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), sl.data_ptr(),
                                      o.data_ptr(), lse.data_ptr(), S, Hq, Hkv, d, bs, mb, kc.shape[0], scale,
                                      stream)
         assert rc == 0, eta.attn_status_string(rc)
         torch.cuda.synchronize()
         assert eta.attn_get_device_error() == 0
-        _compare(o, lse, o_ref, lse_ref)
+        free.append(torch.cuda.mem_get_info()[0])
+        _compare(o, lse, o_ws, lse_ws)
+        check_attention(o, lse, o_ref, lse_ref, f"noalloc d={d}")
+    assert free[0] == free[1], f"device free memory changed between calls: {free[0]} -> {free[1]}"
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     eta.build()
     lib = eta.load_library()
-    # 64 sequences x 32 query heads x 64 splits (32k context) needs ~65 MiB of partials
-    S, Hq, Hkv, d, bs, mb = 64, 32, 8, 128, 16, 2048
+    # 64 sequences x 32 query heads x 64 splits (32k context) needs ~65 MiB of partials.
+    # Real (small) device buffers: the size check must reject the call before any launch,
+    # and nothing here would let a kernel read past them if it did not.
+    S, Hq, Hkv, d, bs, mb, nblk = 64, 32, 8, 128, 16, 2048, 4
     assert eta.attn_decode_workspace_size(S, Hq, Hkv, d, bs, mb) > 64 << 20
-    fake = 0x7F0000000000
-    rc = lib.attn_decode_noalloc(fake, fake, fake, fake, fake, fake, fake, S, Hq, Hkv, d, bs, mb, 1000, 0.1, None)
+    dev = torch.device("cuda")
+    q = torch.zeros((S, Hq, d), dtype=torch.bfloat16, device=dev)
+    o = torch.zeros_like(q)
+    lse = torch.zeros((S, Hq), dtype=torch.float32, device=dev)
+    kc = torch.zeros((nblk, Hkv, bs, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    bt = torch.zeros((S, mb), dtype=torch.int32, device=dev)
+    sl = torch.ones((S,), dtype=torch.int32, device=dev)
+    rc = lib.attn_decode_noalloc(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), sl.data_ptr(),
+                                 o.data_ptr(), lse.data_ptr(), S, Hq, Hkv, d, bs, mb, nblk, 0.1, None)
     assert rc == -4, eta.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert eta.attn_get_device_error() == 0
+    assert torch.all(o == 0) and torch.all(lse == 0)  # nothing was written
