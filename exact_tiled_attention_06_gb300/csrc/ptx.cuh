@@ -229,12 +229,8 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
-// Shared-memory operand descriptor (tcgen05 format) for a tile stored with the
-// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms.
-//   lbo: byte distance between atoms along the leading dimension
-//   sbo: byte distance between 8-row groups along the strided dimension
 // kind::f8f6f4 forms (8-bit E4M3 operands, fp32 accumulator): one instruction covers a
-// K extent of 32 elements (32 bytes).
+// K extent of 32 elements (32 bytes). D(tmem) (+)= A(smem desc) * B(smem desc).
 __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate)
 {
@@ -245,6 +241,8 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// D(tmem) (+)= A(tmem) * B(smem desc), kind::f8f6f4.
 __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate)
 {
@@ -255,6 +253,11 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// Shared-memory operand descriptor (tcgen05 format) for a tile stored with the
+// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms.
+//   lbo: byte distance between atoms along the leading dimension
+//   sbo: byte distance between 8-row groups along the strided dimension
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
 {
     uint64_t d = 0;
@@ -266,7 +269,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, dense.
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0), fp32
 // accumulator, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
@@ -277,6 +279,9 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
+
+// Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, dense; each operand K-major
+// or MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major)
 {
     return (1u << 4)                                   // accumulator format: fp32
