@@ -99,3 +99,16 @@ def test_invalid_index_sets_error():
     torch.cuda.synchronize()
     assert eta.binding.STATUS_NAMES[eta.attn_get_device_error()] == "ATTN_ERR_DEVICE_BOUNDS"
     assert eta.attn_get_device_error() == 0
+
+
+def test_c7_workload_every_row(oracle):
+    """The benchmark's block-sparse workload at full size (32 heads of 32768 tokens, key
+    block 0 plus the 8 blocks ending at the diagonal, causal): every output element and lse
+    against the oracle."""
+    c = inputs.C7
+    q, k, v, pat = inputs.sparse_config_inputs(c)
+    o, lse = run(q, k, v, pat, c.causal, -1, c.scale)
+    rp, ci = inputs.block_csr(pat)
+    o_ref, lse_ref = oracle.attn_fwd_blocksparse(f64(q), f64(k), f64(v), rp.numpy(), ci.numpy(), c.scale, c.causal,
+                                                 -1)
+    check_attention(o, lse, o_ref, lse_ref, c.name)

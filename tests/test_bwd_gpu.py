@@ -156,13 +156,17 @@ def test_bwd_deterministic_dk_dv():
     assert (a[0].float() - b[0].float()).abs().max().item() <= 2e-2 * a[0].float().abs().max().item()
 
 
-def test_bwd_full_size_invariants():
-    """At the long-causal size (B=1, H=32, N=8192, d=128): sum_j dK_j = 0 for every head
-    (each row of dS sums to zero) and sum_j dV_j = sum_i dO_i (each row of P sums to one)."""
+def test_bwd_full_size_whole_heads_and_invariants(oracle):
+    """At the long-causal size (B=1, H=32, N=8192, d=128), as the bench runs it:
+    - four whole heads (each its own kv head: first, last and two inside) element by
+      element against the oracle's dQ, dK and dV at the stated gradient tolerances;
+    - every head: sum_j dK_j = 0 (each row of dS sums to zero) and sum_j dV_j = sum_i dO_i
+      (each row of P sums to one)."""
     c = inputs.C3
     q, k, v = inputs.prefill_config_inputs(c)
     do = inputs.grad_output(c.B, c.Hq, c.Nq, c.d, seed=c.seed)
-    dq, dk, dv = run_bwd(q, k, v, do, c.causal, c.window, 1.0 / math.sqrt(c.d))
+    scale = 1.0 / math.sqrt(c.d)
+    dq, dk, dv = run_bwd(q, k, v, do, c.causal, c.window, scale)
     dk64, dv64 = dk.double(), dv.double()
     sum_dk = dk64.sum(dim=2)
     assert (sum_dk.abs() <= 1e-2 * dk64.abs().sum(dim=2) + 1e-3).all()
@@ -170,3 +174,11 @@ def test_bwd_full_size_invariants():
     sum_do = do.cuda().double().sum(dim=2)
     assert ((sum_dv - sum_do).abs() <= 1e-2 * dv64.abs().sum(dim=2) + 1e-2).all()
     assert torch.isfinite(dq.float()).all()
+    assert c.Hq == c.Hkv  # one query head per kv head: a head is a whole kv-head group
+    heads = [0, 11, 22, c.Hq - 1]
+    rq, rk, rv = oracle.attn_bwd(f64(q[:, heads]), f64(k[:, heads]), f64(v[:, heads]), f64(do[:, heads]), scale,
+                                 c.causal, c.window)
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    for i, h in enumerate(heads):
+        for name, got, ref in (("dq", dq[:, h], rq[:, i]), ("dk", dk[:, h], rk[:, i]), ("dv", dv[:, h], rv[:, i])):
+            check_grad(got, ref, f"C3 head {h} {name}")

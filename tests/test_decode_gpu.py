@@ -129,17 +129,19 @@ def test_out_of_range_block_id_sets_device_error():
     assert eta.attn_get_device_error() == -7
 
 
-def test_full_c5_sampled_sequences(oracle):
-    """The full decode workload as the bench runs it; sampled sequences against the oracle."""
+def test_full_c5_every_sequence(oracle):
+    """The full decode workload as the bench runs it: all 64 sequences (every query head)
+    against the oracle, eight sequences per oracle call so that its fp64 copies of the
+    cache stay near 2 GB ("Modern attention kernels", "Numerical validation": GQA mapping,
+    paged blocks that cross sequence tails)."""
     c = inputs.C5
     x = inputs.decode_config_inputs(c)
     o, lse = run_decode(x, c.scale)
-    lens = x.seq_lens.numpy()
-    rng = np.random.default_rng(7)
-    seqs = sorted({int(np.argmin(lens)), int(np.argmax(lens))} | set(int(s) for s in rng.integers(0, c.num_seqs, 3)))
-    o_ref, lse_ref = oracle_decode(oracle, x, c.scale, seqs)
-    check_attention(o.cpu()[seqs], lse.cpu()[seqs], o_ref, lse_ref, "C5 sampled")
-    assert torch.all(torch.isfinite(o))
+    o, lse = o.cpu(), lse.cpu()
+    for s0 in range(0, c.num_seqs, 8):
+        seqs = list(range(s0, min(s0 + 8, c.num_seqs)))
+        o_ref, lse_ref = oracle_decode(oracle, x, c.scale, seqs)
+        check_attention(o[seqs], lse[seqs], o_ref, lse_ref, f"C5 sequences {seqs[0]}-{seqs[-1]}")
 
 
 def test_more_sequences_than_one_launch_holds(oracle):

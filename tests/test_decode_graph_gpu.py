@@ -140,9 +140,9 @@ def test_graph_reports_bad_block_id():
     g.close()
 
 
-def test_full_c8_step_sampled(oracle):
+def test_full_c8_step_every_layer(oracle):
     """The decode-step workload the bench replays: every layer's output against attn_decode
-    bitwise, and sampled sequences of three layers against the oracle."""
+    bitwise, and every sequence of every layer against the oracle."""
     c = inputs.C8
     x = inputs.decode_step_config_inputs(c)
     qs, ks, vs, bt, sl = to_cuda(x)
@@ -154,10 +154,9 @@ def test_full_c8_step_sampled(oracle):
     ref = eager(qs, ks, vs, bt, sl, scale)
     for l in range(c.n_layers):
         assert torch.equal(g.out[l], ref[l][0]) and torch.equal(g.lse[l], ref[l][1])
-    seqs = [0, 3, 7]
-    for l in (0, 15, 31):
-        o_ref, lse_ref = oracle_decode(oracle, x.layer(l), scale, seqs=seqs)
-        check_attention(g.out[l][seqs], g.lse[l][seqs], o_ref, lse_ref, f"C8 layer {l}")
+    for l in range(c.n_layers):
+        o_ref, lse_ref = oracle_decode(oracle, x.layer(l), scale)
+        check_attention(g.out[l], g.lse[l], o_ref, lse_ref, f"C8 layer {l}")
     g.close()
 
 

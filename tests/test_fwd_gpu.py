@@ -147,27 +147,13 @@ def test_deterministic_and_stream_aware():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def _sample_rows(N, H, rng, extra=12):
-    rows = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1}
-    rows |= set(int(x) for x in rng.integers(0, N, extra))
-    heads = {0, H - 1, int(rng.integers(0, H))}
-    return sorted(rows), sorted(heads)
-
-
 @pytest.mark.parametrize("cfg", [inputs.C2, inputs.C3, inputs.C4], ids=lambda c: c.name)
-def test_full_size_sampled_rows(oracle, cfg):
-    """Full workload in the bench's launch configuration; sampled rows against the oracle."""
+def test_full_size_every_row(oracle, cfg):
+    """Full workload in the bench's launch configuration: every output element and every
+    lse of every head against the oracle ("Modern attention kernels", "Numerical
+    validation": long rows with large logit ranges, GQA mapping; C3 also moves the running
+    max late in many rows through its doubled K rows)."""
     q, k, v = inputs.prefill_config_inputs(cfg)
     o, lse = run_fwd(q, k, v, cfg.causal, cfg.window)
-    o, lse = o.cpu(), lse.cpu()
-    rng = np.random.default_rng(12)
-    G = cfg.Hq // cfg.Hkv
-    for b in sorted({0, cfg.B - 1}):
-        rows, heads = _sample_rows(cfg.Nq, cfg.Hq, rng)
-        for h in heads:
-            hk = h // G
-            qs, ks, vs = f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, hk:hk + 1]), f64(v[b:b + 1, hk:hk + 1])
-            sel = np.array([[0, 0, i] for i in rows])
-            o_ref, lse_ref = oracle.attn_fwd_rows(qs, ks, vs, sel, cfg.scale, cfg.causal, cfg.window)
-            check_attention(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"{cfg.name} b={b} h={h}")
-    assert torch.all(torch.isfinite(o)) and torch.all(torch.isfinite(lse))
+    o_ref, lse_ref = oracle.attn_fwd(f64(q), f64(k), f64(v), cfg.scale, cfg.causal, cfg.window)
+    check_attention(o, lse, o_ref, lse_ref, cfg.name)
