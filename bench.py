@@ -186,19 +186,22 @@ def load_traffic(kernel: str):
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi; ``mark()`` brackets the
-    timed region so that only samples taken inside it are summarised."""
+    """Samples SM clocks and throttle reasons with nvidia-smi while the benchmark runs.
+    ``mark()`` brackets the timed step region and ``window(name)`` each further timed loop;
+    the summary covers the samples taken inside those windows (the step region's own
+    samples are reported separately, since a short step region may hold only a few)."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, interval_ms: int = 50):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.gpu = gpu_index
         self.interval = interval_ms
         self.proc = None
         self.path = None
         self.t0 = self.t1 = None
+        self.windows = []  # (name, start, end) of the timed loops after the step
 
     def __enter__(self):
         try:
@@ -208,6 +211,8 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
+            import atexit
+            atexit.register(self.__exit__, None, None, None)  # never leave the sampler running
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -219,8 +224,11 @@ class ClockSampler:
         else:
             self.t1 = time.time()
 
+    def window(self, name: str, start: float, end: float):
+        self.windows.append((name, start, end))
+
     def __exit__(self, *exc):
-        if self.proc is not None:
+        if self.proc is not None and self.proc.returncode is None and not self.out.closed:
             time.sleep(0.2)
             self.proc.terminate()
             try:
@@ -239,7 +247,7 @@ class ClockSampler:
         except Exception:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        inside, everything = [], []
+        step, timed, everything = [], [], []
         for r in rows:
             if len(r) < 10:
                 continue
@@ -250,15 +258,20 @@ class ClockSampler:
             except ValueError:
                 continue
             everything.append(rec)
-            if self.t0 is not None and self.t1 is not None and self.t0 <= ts <= self.t1:
-                inside.append(rec)
-        use = inside or everything
+            in_step = self.t0 is not None and self.t1 is not None and self.t0 <= ts <= self.t1
+            if in_step:
+                step.append(rec)
+            if in_step or any(a <= ts <= b for _, a, b in self.windows):
+                timed.append(rec)
+        use = timed or everything
         if not use:
             return None
         reasons = sorted({n for rec in use for n in rec[2]})
         power = [rec[3] for rec in use if rec[3] is not None]
         return {"sm_mhz": float(np.median([rec[0] for rec in use])), "sm_max_mhz": float(max(rec[1] for rec in use)),
-                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(step),
+                "step_region_sm_mhz": float(np.median([rec[0] for rec in step])) if step else None,
+                "timed_loops": len(self.windows), "interval_ms": self.interval,
                 "power_w_max": max(power) if power else None}
 
 
@@ -321,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
         kv_bytes = decode_kv_bytes(dx.seq_lens.numpy(), dc.Hkv, dc.d)
         part = Part("decode", host, (do, dlse), run_decode, kv_bytes, 1e9, "GB/s", 1)
         part.extra = {"num_seqs": S, "sum_seq_len": int(dx.seq_lens.sum()), "workspace_bytes": int(ws.numel()),
-                      "workspace": ws}
+                      "workspace": ws, "seq_lens": dx.seq_lens.tolist()}
         parts.append(part)
 
     for p in parts:
@@ -344,17 +357,19 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clocks:
-        clocks.mark(True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            for j, p in enumerate(parts):
-                ev[i][j][0].record(stream)
-                p.run(p.dev)
-                ev[i][j][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        clocks.mark(False)
+    clocks = ClockSampler(local_rank).__enter__()  # runs until every timed loop below is done
+    clocks.mark(True)
+    torch.cuda.nvtx.range_push("timed step")
+    t_start.record(stream)
+    for i in range(args.steps):
+        for j, p in enumerate(parts):
+            ev[i][j][0].record(stream)
+            p.run(p.dev)
+            ev[i][j][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    clocks.mark(False)
     if world > 1:
         dist.barrier()
     err = eta.attn_get_device_error()
@@ -403,30 +418,46 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed e2e step")
         for i in range(e2e_steps):
             e2e_step(i)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         e2e_ms = [float(np.mean([e_ev[i][j][0].elapsed_time(e_ev[i][j][1]) for i in range(e2e_steps)]))
                   for j in range(len(parts))]
 
     def timed_loop(run, what):
-        """W untimed calls, then K calls each bracketed by CUDA events on the launching
+        """W untimed calls, then at least K calls (and at least --min-loop-seconds of them,
+        so the clock sampler sees the loop) each bracketed by CUDA events on the launching
         stream, between barriers; the device error word is checked after both."""
-        for _ in range(args.warmup):
+        for _ in range(max(args.warmup, 1)):
             run()
         torch.cuda.synchronize()
         err = eta.attn_get_device_error()
         if err != 0:
             raise RuntimeError(f"device error in the {what} warm-up: {eta.attn_status_string(err)}")
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(3):
+            run()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        est_ms = max(c0.elapsed_time(c1) / 3, 1e-3)
+        reps = int(max(args.steps, min(math.ceil(args.min_loop_seconds * 1e3 / est_ms), 100000)))
+        reps = int(reduce_max([reps], world, dev)[0])  # every rank times the same count
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push(f"timed {what}")
+        w0 = time.time()
         for e0, e1 in evs:
             e0.record(stream)
             run()
             e1.record(stream)
         torch.cuda.synchronize()
+        clocks.window(what, w0, time.time())
+        torch.cuda.nvtx.range_pop()
         if world > 1:
             dist.barrier()
         err = eta.attn_get_device_error()
@@ -531,12 +562,33 @@ def run_ours(args, rank, world, local_rank):
         graph_ms = timed_loop(run_graph, "graph decode step")
         graph.close()
 
+    # ---- the other prefill workloads (the pages' check shape C1, C2, C4): attn_fwd in a
+    #      loop of its own each (C2 and C4 inputs exceed L2; C1 is a latency case of 4
+    #      blocks whose inputs stay in L2, reported without a roofline target)
+    cfg_ms = {}
+    if args.workload in ("both", "prefill") and not args.no_other_prefill:
+        for cfg in (inputs.C1, inputs.C2, inputs.C4):
+            xq, xk, xv = (t.to(dev) for t in inputs.prefill_config_inputs(cfg, seed=cfg.seed + rank))
+            xo = torch.empty(xq.shape, dtype=torch.bfloat16, device=dev)
+            xl = torch.empty(xq.shape[:3], dtype=torch.float32, device=dev)
+
+            def run_cfg(cfg=cfg, xq=xq, xk=xk, xv=xv, xo=xo, xl=xl):
+                eta.attn_fwd(xq, xk, xv, causal=cfg.causal, window=cfg.window, scale=cfg.scale, out=xo, lse=xl)
+
+            cfg_ms[cfg.name] = (cfg, timed_loop(run_cfg, cfg.name))
+            del xq, xk, xv, xo, xl
+    clocks.__exit__(None, None, None)
+
     # ---- max over ranks
     extra = ([float(bwd_ms.mean())] if bwd_ms is not None else []) + ([float(pp_ms.mean())] if pp_ms is not None else [])
     extra += [float(bs_ms.mean())] if bs_ms is not None else []
     extra += [float(eager_ms.mean()), float(graph_ms.mean())] if graph_ms is not None else []
     extra += [float(f8_ms.mean())] if f8_ms is not None else []
+    extra += [float(ms.mean()) for _, ms in cfg_ms.values()]
     vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms + extra, world, dev)
+    cfg_means = {}
+    for name in reversed(list(cfg_ms)):
+        cfg_means[name] = vals.pop()
     f8_mean = vals.pop() if f8_ms is not None else None
     graph_mean = vals.pop() if graph_ms is not None else None
     eager_mean = vals.pop() if graph_ms is not None else None
@@ -635,7 +687,8 @@ def run_ours(args, rank, world, local_rank):
             "workload": ppc.name, "flops_per_launch": pp_flops, "steps": args.steps, "warmup": args.warmup,
             "gpu_launches": args.steps,
             "config": {"num_seqs": ppc.num_seqs, "Hq": ppc.Hq, "Hkv": ppc.Hkv, "d": ppc.d,
-                       "block_size": ppc.block_size, "q_len": ppc.q_len, "kv_lens": px.kv_lens.tolist(),
+                       "block_size": ppc.block_size, "q_len": ppc.q_len,
+                       "kv_len_sum_min_max": [int(px.kv_lens.sum()), int(px.kv_lens.min()), int(px.kv_lens.max())],
                        "causal": ppc.causal},
             "roofline": {"kernel": "attn_fwd_sm103<128, paged>", "bound": "tensor", "achieved": round(achieved, 2),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -691,7 +744,8 @@ def run_ours(args, rank, world, local_rank):
             "per_call_value": round(whole_job_rate(g_kv, world, eager_mean, 1e9), 2),
             "graph_speedup": round(eager_mean / graph_mean, 3),
             "config": {"n_layers": gc.n_layers, "num_seqs": gc.num_seqs, "Hq": gc.Hq, "Hkv": gc.Hkv, "d": gc.d,
-                       "block_size": gc.block_size, "seq_lens": gx.seq_lens.tolist()},
+                       "block_size": gc.block_size,
+                       "seq_len_sum_min_max": [int(gx.seq_lens.sum()), int(gx.seq_lens.min()), int(gx.seq_lens.max())]},
             "roofline": {"kernel": "attn_decode_sm103<128> (x n_layers, one graph)", "bound": "hbm",
                          "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} HBM copy",
@@ -699,6 +753,32 @@ def run_ours(args, rank, world, local_rank):
                          "ms_per_step": round(graph_mean, 4),
                          "ms_p10_p50_p90": [round(float(np.percentile(graph_ms, x)), 4) for x in (10, 50, 90)]},
         }
+    details = {"workloads": "per-sequence lengths of the paged workloads timed in the bench line (seeded draws)"}
+    if pp_ms is not None:
+        details[ppc.name] = {"kv_lens": px.kv_lens.tolist(), "q_lens": px.q_lens.tolist()}
+    if graph_ms is not None:
+        details[gc.name] = {"seq_lens": gx.seq_lens.tolist()}
+    if len(parts) > 1:
+        details[dc.name] = {"seq_lens": parts[1].extra["seq_lens"]}
+    result["_details"] = details
+    if cfg_ms:
+        other = {}
+        for name, (cfg, ms) in cfg_ms.items():
+            mean = cfg_means[name]
+            flops = attention_flops(cfg.B, cfg.Hq, cfg.Nq, cfg.Nk, cfg.d, cfg.causal, cfg.window)
+            achieved = flops / (mean * 1e-3) / 1e12
+            kernel = f"attn_fwd_sm103<{cfg.d}>"
+            other[name] = {
+                "value": round(whole_job_rate(flops, world, mean, 1e12), 2), "unit": "TFLOP/s",
+                "flops_per_launch": flops, "launches_timed": int(len(ms)),
+                "roofline": {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 2),
+                             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": round(achieved / peaks["bf16_tflops"], 4),
+                             "traffic": load_traffic("attn_fwd_sm103_" + name.split("_")[0].lower()),
+                             "ms_per_launch": round(mean, 5),
+                             "ms_p10_p50_p90": [round(float(np.percentile(ms, x)), 5) for x in (10, 50, 90)]},
+            }
+        result["prefill_configs"] = other
     return result
 
 
@@ -795,6 +875,12 @@ def main():
                     help="skip the many-layer decode step (per-call launches against one CUDA-graph replay)")
     ap.add_argument("--no-blocksparse", action="store_true", help="skip the block-sparse prefill measurement")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (E4M3) prefill measurement")
+    ap.add_argument("--no-other-prefill", action="store_true",
+                    help="skip the C1, C2 and C4 prefill measurements")
+    ap.add_argument("--min-loop-seconds", type=float, default=0.5,
+                    help="each timed loop after the step runs at least this long (and at least --steps calls)")
+    ap.add_argument("--details", default=os.path.join(ROOT, "bench_details.json"),
+                    help="file for the per-sequence lengths of the paged workloads (kept out of the JSON line)")
     ap.add_argument("--decode-seqs", type=int, default=None,
                     help="profiling aid: fewer decode sequences than the workload's 64")
     args = ap.parse_args()
@@ -819,6 +905,14 @@ def main():
         import torch.distributed as dist
         dist.destroy_process_group()
     if rank == 0 and result is not None:
+        details = result.pop("_details", None)
+        if details is not None and args.details:
+            try:
+                with open(args.details, "w") as f:
+                    json.dump(details, f)
+                result["details_file"] = os.path.relpath(args.details, ROOT)
+            except OSError:
+                pass
         result["cpu_baseline"] = cpu_baseline_entry(sample) if sample else None
         print(json.dumps(result), flush=True)
 
