@@ -157,10 +157,8 @@ __device__ __forceinline__ bool tile_active(const TileWork& t, int j)
     return t.rows > 0 && t.kv_lo <= j && j < t.kv_hi;
 }
 
-// 200 registers per thread: 320 threads x 200 fit the SM's 64K registers with one block
-// per SM (the launch-bounds heuristic stopped at 168 and spilled the softmax's score row).
 template <int D, int MODE>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
 {
