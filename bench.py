@@ -157,6 +157,9 @@ KERNEL_SOURCES = {
     "attn_fwd_sm103_sparse": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_fwd_sm103_fp8": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
     "attn_decode_sm103_c8_step": ("decode_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_fwd_sm103_c1": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_fwd_sm103_c2": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
+    "attn_fwd_sm103_c4": ("fwd_kernel.cu", "ptx.cuh", "internal.h"),
 }
 
 
@@ -859,6 +862,31 @@ def run_reference(args):
     }
 
 
+def summary_of(result):
+    """One short entry per timed workload: [value, unit, roofline fraction, DRAM bytes per
+    launch (null when no current record)], then the clocks seen."""
+    out = {}
+
+    def add(name, block):
+        rf = block.get("roofline", {})
+        out[name] = [block.get("value"), block.get("unit"), rf.get("frac"), rf.get("traffic")]
+
+    add("prefill C3", result)
+    for key, name in (("decode", "decode C5"), ("backward", "backward C3"), ("paged_prefill", "paged prefill C6"),
+                      ("blocksparse", "block-sparse C7"), ("fp8_prefill", "FP8 prefill C3"),
+                      ("decode_graph", "decode step C8 (graph)")):
+        if key in result:
+            add(name, result[key])
+    for name, block in result.get("prefill_configs", {}).items():
+        add("prefill " + name.split("_")[0], block)
+    if "e2e" in result:
+        out["e2e"] = [result["e2e"]["value"], result["e2e"]["unit"], result["e2e"].get("decode_value"),
+                      result["e2e"].get("decode_unit")]
+    c = result.get("clocks") or {}
+    out["clocks"] = [c.get("sm_mhz"), c.get("sm_max_mhz"), c.get("reasons"), c.get("samples")]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -914,6 +942,7 @@ def main():
             except OSError:
                 pass
         result["cpu_baseline"] = cpu_baseline_entry(sample) if sample else None
+        result["summary"] = summary_of(result)  # last key: stays in a record that keeps the line's tail
         print(json.dumps(result), flush=True)
 
 
