@@ -578,7 +578,36 @@ def run_ours(args, rank, world, local_rank):
             def run_cfg(cfg=cfg, xq=xq, xk=xk, xv=xv, xo=xo, xl=xl):
                 eta.attn_fwd(xq, xk, xv, causal=cfg.causal, window=cfg.window, scale=cfg.scale, out=xo, lse=xl)
 
-            cfg_ms[cfg.name] = (cfg, timed_loop(run_cfg, cfg.name))
+            if args.only_config and not cfg.name.startswith(args.only_config):
+                continue
+            per_call = timed_loop(run_cfg, cfg.name)
+            # the same launches replayed from a captured graph (100 per replay): the kernel's
+            # own time without the host's per-call cost, which dominates the 4-block C1
+            graph_ms = None
+            try:
+                if args.no_graph_replay:
+                    raise RuntimeError("skipped")
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for _ in range(100):
+                        run_cfg()
+                g.replay()
+                torch.cuda.synchronize()
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 10
+                g0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                g1.record(stream)
+                torch.cuda.synchronize()
+                graph_ms = g0.elapsed_time(g1) / (reps * 100)
+                del g
+            except Exception:
+                graph_ms = None
+            err = eta.attn_get_device_error()
+            if err != 0:
+                raise RuntimeError(f"device error in the {cfg.name} graph replay: {eta.attn_status_string(err)}")
+            cfg_ms[cfg.name] = (cfg, per_call, graph_ms)
             del xq, xk, xv, xo, xl
     clocks.__exit__(None, None, None)
 
@@ -587,7 +616,7 @@ def run_ours(args, rank, world, local_rank):
     extra += [float(bs_ms.mean())] if bs_ms is not None else []
     extra += [float(eager_ms.mean()), float(graph_ms.mean())] if graph_ms is not None else []
     extra += [float(f8_ms.mean())] if f8_ms is not None else []
-    extra += [float(ms.mean()) for _, ms in cfg_ms.values()]
+    extra += [float(v[1].mean()) for v in cfg_ms.values()]
     vals = reduce_max([total_ms] + [float(m.mean()) for m in part_ms] + e2e_ms + extra, world, dev)
     cfg_means = {}
     for name in reversed(list(cfg_ms)):
@@ -766,7 +795,7 @@ def run_ours(args, rank, world, local_rank):
     result["_details"] = details
     if cfg_ms:
         other = {}
-        for name, (cfg, ms) in cfg_ms.items():
+        for name, (cfg, ms, gms) in cfg_ms.items():
             mean = cfg_means[name]
             flops = attention_flops(cfg.B, cfg.Hq, cfg.Nq, cfg.Nk, cfg.d, cfg.causal, cfg.window)
             achieved = flops / (mean * 1e-3) / 1e12
@@ -774,6 +803,9 @@ def run_ours(args, rank, world, local_rank):
             other[name] = {
                 "value": round(whole_job_rate(flops, world, mean, 1e12), 2), "unit": "TFLOP/s",
                 "flops_per_launch": flops, "launches_timed": int(len(ms)),
+                "graph_replay": None if gms is None else {
+                    "ms_per_launch": round(gms, 5), "value": round(flops / (gms * 1e-3) / 1e12, 2),
+                    "frac": round(flops / (gms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
                 "roofline": {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 2),
                              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                              "frac": round(achieved / peaks["bf16_tflops"], 4),
@@ -879,6 +911,9 @@ def summary_of(result):
             add(name, result[key])
     for name, block in result.get("prefill_configs", {}).items():
         add("prefill " + name.split("_")[0], block)
+        g = block.get("graph_replay")
+        if g:
+            out["prefill " + name.split("_")[0] + " (graph)"] = [g["value"], block.get("unit"), g["frac"]]
     if "e2e" in result:
         out["e2e"] = [result["e2e"]["value"], result["e2e"]["unit"], result["e2e"].get("decode_value"),
                       result["e2e"].get("decode_unit")]
@@ -907,6 +942,10 @@ def main():
                     help="skip the C1, C2 and C4 prefill measurements")
     ap.add_argument("--min-loop-seconds", type=float, default=0.5,
                     help="each timed loop after the step runs at least this long (and at least --steps calls)")
+    ap.add_argument("--only-config", default=None, choices=["C1", "C2", "C4"],
+                    help="profiling aid: of the C1 / C2 / C4 prefill loops run only this one")
+    ap.add_argument("--no-graph-replay", action="store_true",
+                    help="profiling aid: skip the graph-replayed timing of the C1 / C2 / C4 loops")
     ap.add_argument("--details", default=os.path.join(ROOT, "bench_details.json"),
                     help="file for the per-sequence lengths of the paged workloads (kept out of the JSON line)")
     ap.add_argument("--decode-seqs", type=int, default=None,
