@@ -583,7 +583,7 @@ def run_ours(args, rank, world, local_rank):
             per_call = timed_loop(run_cfg, cfg.name)
             # the same launches replayed from a captured graph (100 per replay): the kernel's
             # own time without the host's per-call cost, which dominates the 4-block C1
-            graph_ms = None
+            cfg_graph_ms = None
             try:
                 if args.no_graph_replay:
                     raise RuntimeError("skipped")
@@ -600,14 +600,14 @@ def run_ours(args, rank, world, local_rank):
                     g.replay()
                 g1.record(stream)
                 torch.cuda.synchronize()
-                graph_ms = g0.elapsed_time(g1) / (reps * 100)
+                cfg_graph_ms = g0.elapsed_time(g1) / (reps * 100)
                 del g
             except Exception:
-                graph_ms = None
+                cfg_graph_ms = None
             err = eta.attn_get_device_error()
             if err != 0:
                 raise RuntimeError(f"device error in the {cfg.name} graph replay: {eta.attn_status_string(err)}")
-            cfg_ms[cfg.name] = (cfg, per_call, graph_ms)
+            cfg_ms[cfg.name] = (cfg, per_call, cfg_graph_ms)
             del xq, xk, xv, xo, xl
     clocks.__exit__(None, None, None)
 
