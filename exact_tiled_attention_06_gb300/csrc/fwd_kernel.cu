@@ -98,7 +98,8 @@ struct FwdParams {
     const int32_t* col_idx;      // sparse: listed key blocks, ascending per query block (device)
     float scale_log2;  // scale * log2(e)
     int causal, window;
-    int pair_heads;    // 1: tiles are query heads (2u, 2u+1) at one row tile; 0: row tiles (2r, 2r+1)
+    int pair_heads;    // 1: tiles are query heads (2u, 2u+1) at one row tile; 0: row tiles (2r, 2r+1);
+                       // 2: one tile per block (row tile r of head u), for grids smaller than the GPU
     int n_row_units;   // row units per (batch, head unit)
     int n_hunits;      // head units per batch entry
     int next_stride;   // dense / sparse: units between a block and the one that will take its SM
@@ -207,7 +208,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
     }
     TileWork tw[2];
-    if (p.pair_heads) {
+    if (p.pair_heads == 2) {
+        tw[0] = make_tile(p, hu, ru * BM, nq, nk);
+        tw[1] = TileWork{hu, 0, 0, 0, 0};
+    } else if (p.pair_heads) {
         tw[0] = make_tile(p, 2 * hu, ru * BM, nq, nk);
         tw[1] = make_tile(p, 2 * hu + 1, ru * BM, nq, nk);
     } else {
@@ -426,7 +430,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     const int bh2 = u2 % n_bh;
                     const int b2 = bh2 / p.n_hunits, hu2 = bh2 % p.n_hunits;
                     TileWork t2[2];
-                    if (p.pair_heads) {
+                    if (p.pair_heads == 2) {
+                        t2[0] = make_tile(p, hu2, ru2 * BM, p.Nq, p.Nk);
+                        t2[1] = TileWork{hu2, 0, 0, 0, 0};
+                    } else if (p.pair_heads) {
                         t2[0] = make_tile(p, 2 * hu2, ru2 * BM, p.Nq, p.Nk);
                         t2[1] = make_tile(p, 2 * hu2 + 1, ru2 * BM, p.Nq, p.Nk);
                     } else {
@@ -893,6 +900,13 @@ int launch_fwd_d(const void* q, const void* k, const void* v, void* o, float* ls
     prm.next_stride = sm_count();  // one block per SM: the block launched next is about this far on
     prm.out_scale = 1.0f;
     prm.err = err;
+    if (2 * static_cast<long long>(B) * prm.n_hunits * prm.n_row_units <= prm.next_stride) {
+        // a grid of at most half the SMs: one query tile per block instead (still one wave),
+        // so the tiles run side by side
+        prm.pair_heads = 2;
+        prm.n_row_units = n_row_tiles;
+        prm.n_hunits = Hq;
+    }
     const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
     if (grid > INT_MAX) return kErrInvalidArg;
@@ -969,6 +983,11 @@ int launch_fwd_fp8_128(const void* q, const void* k, const void* vt, void* o, fl
     prm.next_stride = sm_count();
     prm.out_scale = v_descale;
     prm.err = err;
+    if (2 * static_cast<long long>(B) * prm.n_hunits * prm.n_row_units <= prm.next_stride) {
+        prm.pair_heads = 2;  // a grid of at most half the SMs: one query tile per block (one wave)
+        prm.n_row_units = n_row_tiles;
+        prm.n_hunits = Hq;
+    }
     const long long grid = static_cast<long long>(B) * prm.n_hunits * prm.n_row_units;
     if (grid <= 0) return kOk;
     if (grid > INT_MAX) return kErrInvalidArg;

@@ -112,3 +112,9 @@ def test_c7_workload_every_row(oracle):
     o_ref, lse_ref = oracle.attn_fwd_blocksparse(f64(q), f64(k), f64(v), rp.numpy(), ci.numpy(), c.scale, c.causal,
                                                  -1)
     check_attention(o, lse, o_ref, lse_ref, c.name)
+
+
+def test_random_pattern_paired_blocks(oracle):
+    """160 heads keep two query tiles per block (small grids run one per block)."""
+    pat = inputs.random_pattern(8, 8, 0.5, seed=160, empty_rows=(3,))
+    case(oracle, 1, 160, 160, 900, 900, 128, True, -1, pat, seed=160, what="160 heads")

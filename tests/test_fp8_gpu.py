@@ -144,6 +144,13 @@ def test_fp8_float8_dtype_accepted():
     assert torch.equal(o1, o2)
 
 
+def test_fp8_paired_blocks(oracle):
+    """160 heads keep two query tiles per block (small grids run one per block)."""
+    x = inputs.fp8_prefill_inputs(1, 160, 160, 300, 304, 128, seed=160)
+    o, lse = run(x, True)
+    check_fp8(oracle, x, o, lse, True, what="160 heads")
+
+
 def test_fp8_full_long_causal_every_row(oracle):
     """The long causal workload (B1 H32 N8192 d128, 1 % of K rows doubled) in E4M3, as the
     bench times it: every row of every head against the oracle on the decoded values, with

@@ -49,6 +49,20 @@ def test_boundary_sweep(oracle, N, d, causal, window):
     case(oracle, 1, 2, 1, N, N, d, causal, window, seed=N + d, what=f"N={N} d={d} c={causal} w={window}")
 
 
+# Grids of at most half the SMs run one query tile per block; with 160 heads the same
+# ragged shapes keep two tiles per block (row tiles 2r, 2r + 1 of a head, or two heads of a
+# kv head), so both launch forms see every boundary case.
+@pytest.mark.parametrize("N", [1, 65, 129, 257, 1000])
+@pytest.mark.parametrize("causal,window", [(False, -1), (True, -1), (True, 129), (False, 129)])
+def test_boundary_sweep_paired_blocks(oracle, N, causal, window):
+    case(oracle, 1, 160, 160, N, N, 128, causal, window, seed=N + 7, what=f"160 heads N={N} c={causal} w={window}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(96, 32), (128, 32)])
+def test_gqa_paired_blocks(oracle, Hq, Hkv):
+    case(oracle, 1, Hq, Hkv, 300, 300, 128, True, -1, seed=Hq + Hkv, what=f"GQA {Hq}/{Hkv} paired blocks")
+
+
 @pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 100), (1, 1000), (129, 1), (200, 257)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_rectangular(oracle, Nq, Nk, causal):
