@@ -58,7 +58,14 @@ def test_boundary_sweep_paired_blocks(oracle, N, causal, window):
     case(oracle, 1, 160, 160, N, N, 128, causal, window, seed=N + 7, what=f"160 heads N={N} c={causal} w={window}")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(96, 32), (128, 32)])
+@pytest.mark.parametrize("Nq,Nk", [(300, 100), (1000, 300), (300, 1000)])
+def test_rectangular_many_heads(oracle, Nq, Nk):
+    """Bottom-right causal alignment over many blocks: with Nq > Nk the leading rows see no
+    key and must come out as O = 0, lse = -inf."""
+    case(oracle, 1, 160, 160, Nq, Nk, 128, True, -1, seed=Nq + 3 * Nk, what=f"160 heads {Nq}x{Nk}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(96, 32), (128, 32), (256, 64), (192, 64)])
 def test_gqa_paired_blocks(oracle, Hq, Hkv):
     case(oracle, 1, Hq, Hkv, 300, 300, 128, True, -1, seed=Hq + Hkv, what=f"GQA {Hq}/{Hkv} paired blocks")
 
