@@ -124,6 +124,146 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p)
     return *reinterpret_cast<const uint32_t*>(p);
 }
 
+// Merge of one (sequence, head group)'s chunk partials for the column slice
+// [tw S, (tw + 1) S), S = 32 VEC: eight lanes per query head (four heads at a time), each
+// lane owning VEC float4 (4 VEC consecutive columns) of the slice. The chunks' log-sums
+// are spread over a head's eight lanes (chunk c on lane c % 8, up to 64 chunks held in
+// registers) and reduced there; their weights reach the other lanes by shuffle. A lane
+// holds kLoads float4 of partial rows at once, kLoads / VEC chunks, so the rows of up to
+// 4 (VEC 4), 16 (VEC 2) or 32 (VEC 1) chunks arrive in one round trip; the first group is
+// requested before the log-sums.
+template <int D, int VEC>
+__device__ __forceinline__ void merge_slice(const DecParams& p, int seq, int hq0, int nvalid, int n_splits, int tw,
+                                            int lane)
+{
+    constexpr int kCols = 4 * VEC;     // this lane's columns
+    constexpr int kSlice = 8 * kCols;  // the slice's columns
+    // float4 of partial rows a lane holds at once: 32 for a team's narrow slice (a small
+    // batch: its merges end the launch, one round trip matters), 16 for a whole row (a large
+    // batch: merges overlap other warps' streaming, fewer registers in flight measured better)
+    constexpr int kLoads = VEC == 4 ? 16 : 32;
+    constexpr int kGroup = kLoads / VEC;  // chunks per group of loads
+    constexpr int kRun = kGroup < 8 ? kGroup : 8;  // chunks whose weights one register holds
+    static_assert(kGroup % kRun == 0 && 8 % kRun == 0, "weight runs tile the group");
+    constexpr int kHeld = 8;           // log-sums per lane in registers
+    static_assert(kSlice <= D, "slice within the head");
+    const int slot_row = lane >> 3;    // head within the group of four
+    const int cg = lane & 7;           // column group (and chunk c = cg mod 8)
+    const int src0 = slot_row * 8;
+    const size_t split_stride = static_cast<size_t>(p.num_seqs) * p.Hq;  // rows per chunk
+    const size_t cstride = split_stride * (D / 4);                       // float4 per chunk
+    for (int rb = 0; rb < nvalid; rb += 4) {
+        const int row = rb + slot_row;
+        const bool live = row < nvalid;
+        const size_t r0 = static_cast<size_t>(seq) * p.Hq + hq0 + (live ? row : nvalid - 1);
+        const float* lse_r = p.part_lse + r0;
+        const int col0 = tw * kSlice + cg * kCols;
+        const float4* po = reinterpret_cast<const float4*>(p.part_o + r0 * D + col0);
+        float acc[kCols];
+#pragma unroll
+        for (int t = 0; t < kCols; ++t) acc[t] = 0.0f;
+        float4 v[kGroup][VEC];
+        auto load_group = [&](int c) {
+#pragma unroll
+            for (int k = 0; k < kGroup; ++k)
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    v[k][j] = c + k < n_splits ? __ldcg(po + (c + k) * cstride + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        // chunks r kRun .. r kRun + kRun - 1 of the loaded group, weights from register hreg
+        // of lanes src0 + off .. src0 + off + kRun - 1
+        auto add_run = [&](int r, float hreg, int off) {
+#pragma unroll
+            for (int k = 0; k < kRun; ++k) {
+                const float w = __shfl_sync(0xffffffffu, hreg, src0 + off + k);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float4 x = v[kRun * r + k][j];
+                    acc[4 * j + 0] = fmaf(w, x.x, acc[4 * j + 0]);
+                    acc[4 * j + 1] = fmaf(w, x.y, acc[4 * j + 1]);
+                    acc[4 * j + 2] = fmaf(w, x.z, acc[4 * j + 2]);
+                    acc[4 * j + 3] = fmaf(w, x.w, acc[4 * j + 3]);
+                }
+            }
+        };
+        float M = -INFINITY, S = 0.0f;
+        if (n_splits <= 8 * kHeld) {
+            load_group(0);
+            float hl[kHeld];
+#pragma unroll
+            for (int k = 0; k < kHeld; ++k) {
+                const int c = cg + 8 * k;
+                hl[k] = c < n_splits ? __ldcg(lse_r + c * split_stride) : -INFINITY;
+            }
+#pragma unroll
+            for (int k = 0; k < kHeld; ++k) M = fmaxf(M, hl[k]);
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+#pragma unroll
+            for (int k = 0; k < kHeld; ++k) {
+                hl[k] = ex2_approx(hl[k] - M);  // the chunk's weight (0 past n_splits)
+                S += hl[k];
+            }
+            S += __shfl_xor_sync(0xffffffffu, S, 1);
+            S += __shfl_xor_sync(0xffffffffu, S, 2);
+            S += __shfl_xor_sync(0xffffffffu, S, 4);
+            for (int c = 0; c < n_splits; c += kGroup) {
+                if (c > 0) load_group(c);
+#pragma unroll
+                for (int r = 0; r < kGroup / kRun; ++r) {
+                    const int c0 = c + kRun * r;
+                    if (c0 >= n_splits) break;
+                    const int hb = c0 >> 3;  // register holding these weights
+                    float hreg = hl[0];
+#pragma unroll
+                    for (int j = 1; j < kHeld; ++j)
+                        if (j == hb) hreg = hl[j];
+                    add_run(r, hreg, c0 & 7);
+                }
+            }
+        } else {
+            // more chunks than registers hold: log-sums read twice
+            for (int c = cg; c < n_splits; c += 8) M = fmaxf(M, __ldcg(lse_r + c * split_stride));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+            for (int c = cg; c < n_splits; c += 8) S += ex2_approx(__ldcg(lse_r + c * split_stride) - M);
+            S += __shfl_xor_sync(0xffffffffu, S, 1);
+            S += __shfl_xor_sync(0xffffffffu, S, 2);
+            S += __shfl_xor_sync(0xffffffffu, S, 4);
+            for (int c = 0; c < n_splits; c += kGroup) {
+                load_group(c);
+                float hw[kGroup / kRun];  // lane cg < kRun: weight of chunk c + kRun r + cg
+#pragma unroll
+                for (int r = 0; r < kGroup / kRun; ++r) {
+                    const int ch = c + kRun * r + cg;
+                    hw[r] = cg < kRun && ch < n_splits ? ex2_approx(__ldcg(lse_r + ch * split_stride) - M) : 0.0f;
+                }
+#pragma unroll
+                for (int r = 0; r < kGroup / kRun; ++r) add_run(r, hw[r], 0);
+            }
+        }
+        if (live) {
+            const float inv = 1.0f / S;
+            __nv_bfloat16* ob = p.o + r0 * D + col0;
+            if constexpr (kCols >= 8) {
+                uint4* orow = reinterpret_cast<uint4*>(ob);
+#pragma unroll
+                for (int x = 0; x < kCols / 8; ++x)
+                    orow[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv, acc[8 * x + 1] * inv),
+                                         pack_bf16x2(acc[8 * x + 2] * inv, acc[8 * x + 3] * inv),
+                                         pack_bf16x2(acc[8 * x + 4] * inv, acc[8 * x + 5] * inv),
+                                         pack_bf16x2(acc[8 * x + 6] * inv, acc[8 * x + 7] * inv));
+            } else {
+                *reinterpret_cast<uint2*>(ob) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                           pack_bf16x2(acc[2] * inv, acc[3] * inv));
+            }
+            if (tw == 0 && cg == 0) p.lse[r0] = (M + log2f(S)) * kLn2;
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecWarps * 32, 1)
     attn_decode_sm103(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -668,170 +808,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1)
         if (!last) continue;
         }
         // ---- this warp finished the last chunk of (seq, head group) for its column slice
-        // (all D columns when T = 1): merge that slice of every partial. Eight lanes per
-        // query head (four heads at a time), each lane owning D/8/T consecutive columns.
-        // The chunks' log-sums are spread over a head's eight lanes (chunk c on lane c % 8),
-        // kept in registers and reduced there; their weights reach the other lanes by
-        // shuffle. The partial rows are read in groups of four chunks (eight when the
-        // slice is narrow) with independent 16-byte loads, the first group issued before
-        // the log-sums are reduced.
+        // (all D columns when T = 1): merge that slice of every partial
         __threadfence();
         {
-            constexpr int kCols = D / 8;           // columns per lane at most (16 or 8)
-            constexpr int kVec = kCols / 4;        // float4 loads per lane per chunk at most
-            constexpr int kHeld = 8;               // log-sums per lane: up to 64 chunks in registers
-            const int cols = kCols / T;            // this slice's columns per lane (>= 4)
-            const int vec = cols / 4;
-            const int slot_row = lane >> 3;        // head within the group of four
-            const int cg = lane & 7;               // column group (and chunk c = cg mod 8)
-            const size_t split_stride = static_cast<size_t>(p.num_seqs) * p.Hq;  // rows per chunk
-            for (int rb = 0; rb < nvalid; rb += 4) {
-                const int row = rb + slot_row;
-                const bool live = row < nvalid;
-                const size_t r0 = static_cast<size_t>(seq) * p.Hq + hq0 + (live ? row : nvalid - 1);
-                const float* lse_r = p.part_lse + r0;
-                const int col0 = tw * (D / T) + cg * cols;
-                const float* po = p.part_o + r0 * D + col0;
-                float acc[kCols];
-#pragma unroll
-                for (int t = 0; t < kCols; ++t) acc[t] = 0.0f;
-                auto add4 = [&](const float4 (&v)[kVec], float w) {
-#pragma unroll
-                    for (int x = 0; x < kVec; ++x) {
-                        if (x >= vec) break;
-                        acc[4 * x + 0] = fmaf(w, v[x].x, acc[4 * x + 0]);
-                        acc[4 * x + 1] = fmaf(w, v[x].y, acc[4 * x + 1]);
-                        acc[4 * x + 2] = fmaf(w, v[x].z, acc[4 * x + 2]);
-                        acc[4 * x + 3] = fmaf(w, v[x].w, acc[4 * x + 3]);
-                    }
-                };
-                float M = -INFINITY, S = 0.0f;
-                if (n_splits <= 8 * kHeld) {
-                    // A group of chunks' rows is loaded at once into v[4][kVec]: four chunks,
-                    // or eight when this slice's columns fill at most half a register row
-                    // (chunk c + 4 + k in the upper half). The first group is issued before
-                    // the log-sums are reduced.
-                    const bool wide = 2 * vec <= kVec;
-                    const int gsize = wide ? 8 : 4;
-                    auto load_group = [&](float4 (&v)[4][kVec], int c) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-#pragma unroll
-                            for (int x = 0; x < kVec; ++x) {
-                                const bool up = wide && x >= kVec / 2;
-                                const int ch = c + k + (up ? 4 : 0);
-                                const int xx = up ? x - kVec / 2 : x;
-                                v[k][x] = (ch < n_splits && xx < vec)
-                                    ? __ldcg(reinterpret_cast<const float4*>(po + ch * split_stride * D) + xx)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-                    };
-                    float hl[kHeld];
-                    // weights of chunks c .. c + gsize - 1 come from register hl[c / 8] of lanes
-                    // 8 slot_row + (c % 8) ...
-                    const int src0 = slot_row * 8;
-                    auto add_group = [&](const float4 (&v)[4][kVec], int c, float hreg) {
-                        if (wide) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const float w_lo = __shfl_sync(0xffffffffu, hreg, src0 + (c & 7) + k);
-                                const float w_hi = __shfl_sync(0xffffffffu, hreg, src0 + (c & 7) + 4 + k);
-#pragma unroll
-                                for (int x = 0; x < kVec / 2; ++x) {
-                                    if (x >= vec) break;
-                                    const float4 lo = v[k][x], hi = v[k][kVec / 2 + x];
-                                    acc[4 * x + 0] = fmaf(w_hi, hi.x, fmaf(w_lo, lo.x, acc[4 * x + 0]));
-                                    acc[4 * x + 1] = fmaf(w_hi, hi.y, fmaf(w_lo, lo.y, acc[4 * x + 1]));
-                                    acc[4 * x + 2] = fmaf(w_hi, hi.z, fmaf(w_lo, lo.z, acc[4 * x + 2]));
-                                    acc[4 * x + 3] = fmaf(w_hi, hi.w, fmaf(w_lo, lo.w, acc[4 * x + 3]));
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) add4(v[k], __shfl_sync(0xffffffffu, hreg, src0 + (c & 7) + k));
-                        }
-                    };
-                    float4 v0[4][kVec];
-                    load_group(v0, 0);
-#pragma unroll
-                    for (int k = 0; k < kHeld; ++k) {
-                        const int c = cg + 8 * k;
-                        hl[k] = c < n_splits ? __ldcg(lse_r + c * split_stride) : -INFINITY;
-                    }
-#pragma unroll
-                    for (int k = 0; k < kHeld; ++k) M = fmaxf(M, hl[k]);
-                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-#pragma unroll
-                    for (int k = 0; k < kHeld; ++k) {
-                        hl[k] = ex2_approx(hl[k] - M);  // the chunk's weight (0 past n_splits)
-                        S += hl[k];
-                    }
-                    S += __shfl_xor_sync(0xffffffffu, S, 1);
-                    S += __shfl_xor_sync(0xffffffffu, S, 2);
-                    S += __shfl_xor_sync(0xffffffffu, S, 4);
-                    add_group(v0, 0, hl[0]);
-#pragma unroll
-                    for (int kb = 0; kb < kHeld; ++kb) {
-                        // chunks 8 kb .. 8 kb + 7: one group of eight or two of four
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const int c = 8 * kb + 4 * half;
-                            if (c < gsize) continue;  // in the first group
-                            if (c >= n_splits) break;
-                            if (wide && half == 1) break;  // covered by the group at 8 kb
-                            float4 v[4][kVec];
-                            load_group(v, c);
-                            add_group(v, c, hl[kb]);
-                        }
-                    }
-                } else {
-                    // more chunks than registers hold: log-sums read twice, rows four at a time
-                    for (int c = cg; c < n_splits; c += 8) M = fmaxf(M, __ldcg(lse_r + c * split_stride));
-                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-                    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-                    for (int c = cg; c < n_splits; c += 8) S += ex2_approx(__ldcg(lse_r + c * split_stride) - M);
-                    S += __shfl_xor_sync(0xffffffffu, S, 1);
-                    S += __shfl_xor_sync(0xffffffffu, S, 2);
-                    S += __shfl_xor_sync(0xffffffffu, S, 4);
-                    for (int c = 0; c < n_splits; c += 4) {
-                        const int cn = min(4, n_splits - c);
-                        float lv[4];
-                        float4 v[4][kVec];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            lv[k] = k < cn ? __ldcg(lse_r + (c + k) * split_stride) : -INFINITY;
-#pragma unroll
-                            for (int x = 0; x < kVec; ++x)
-                                v[k][x] = (k < cn && x < vec)
-                                    ? __ldcg(reinterpret_cast<const float4*>(po + (c + k) * split_stride * D) + x)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) add4(v[k], ex2_approx(lv[k] - M));
-                    }
-                }
-                if (live) {
-                    const float inv = 1.0f / S;
-                    __nv_bfloat16* ob = p.o + r0 * D + col0;
-                    if (cols >= 8) {
-                        uint4* orow = reinterpret_cast<uint4*>(ob);
-#pragma unroll
-                        for (int x = 0; x < kCols / 8; ++x)
-                            if (8 * x < cols)
-                                orow[x] = make_uint4(pack_bf16x2(acc[8 * x + 0] * inv, acc[8 * x + 1] * inv),
-                                                     pack_bf16x2(acc[8 * x + 2] * inv, acc[8 * x + 3] * inv),
-                                                     pack_bf16x2(acc[8 * x + 4] * inv, acc[8 * x + 5] * inv),
-                                                     pack_bf16x2(acc[8 * x + 6] * inv, acc[8 * x + 7] * inv));
-                    } else {
-                        *reinterpret_cast<uint2*>(ob) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                                                                   pack_bf16x2(acc[2] * inv, acc[3] * inv));
-                    }
-                    if (tw == 0 && cg == 0) p.lse[r0] = (M + log2f(S)) * kLn2;
-                }
+            const int vec = D / 32 / T;  // float4 per lane of the slice
+            if constexpr (D >= 128) {
+                if (vec == 4) merge_slice<D, 4>(p, seq, hq0, nvalid, n_splits, tw, lane);
             }
+            if (vec == 2) merge_slice<D, 2>(p, seq, hq0, nvalid, n_splits, tw, lane);
+            else if (vec == 1) merge_slice<D, 1>(p, seq, hq0, nvalid, n_splits, tw, lane);
         }
         if (lane == 0) p.done[done_idx] = 0;  // the last to touch it
     }
