@@ -235,6 +235,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t bar_q = bar0;
     auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
     auto kv_empty = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
+    // Copy n of the ring (K and V alternate: n even K_j, odd V_j) may start once copy
+    // n - kStages has been released. bf16: a V tile is released by the commit that releases
+    // the K tile after it, issued once every product of that key step was issued (so after
+    // the V tile's P V products): one commit fewer per key step. FP8, whose steps are
+    // shorter, releases every tile on its own (the later V releases measured slower there).
+    constexpr bool kVByK = !FP8;
+    auto slot_free = [&](int n, int kind) { return kVByK && kind ? kv_empty((n + 1) % C::kStages) : kv_empty(n % C::kStages); };
+    auto slot_free_parity = [&](int n, int kind) {
+        return static_cast<uint32_t>((kVByK && kind ? (n + 1 - C::kStages) / C::kStages : n / C::kStages - 1) & 1);
+    };
     auto s_full = [&](int t) { return bar0 + 8u * (1 + 2 * C::kStages + t); };
     auto p_full = [&](int t) { return bar0 + 8u * (3 + 2 * C::kStages + t); };
     auto o_done = [&](int t) { return bar0 + 8u * (5 + 2 * C::kStages + t); };
@@ -410,7 +420,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int kind = 0; kind < 2; ++kind) {
                         const int s = n % C::kStages;
                         if (n >= C::kStages &&
-                            !mbar_wait(kv_empty(s), ((n / C::kStages) - 1) & 1, abort_flag, p.err)) {
+                            !mbar_wait(slot_free(n, kind), slot_free_parity(n, kind), abort_flag, p.err)) {
                             ok = false;
                             break;
                         }
@@ -499,7 +509,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     const int s = n % C::kStages;
                     bool w = true;
                     if (lane == 0) {
-                        if (n >= C::kStages) w = mbar_wait(kv_empty(s), ((n / C::kStages) - 1) & 1, abort_flag, p.err);
+                        if (n >= C::kStages) w = mbar_wait(slot_free(n, kind), slot_free_parity(n, kind), abort_flag, p.err);
                         if (w)
                             mbar_arrive_expect_tx(kv_full(s), static_cast<uint32_t>(n_sub * sub_rows * 128 * C::kBoxes));
                     }
@@ -653,7 +663,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     first_pv[1] = false;
                     if (e == last_e[1]) tc_commit(o_done(1));
                 }
-                tc_commit(kv_empty(vs));
+                if constexpr (!kVByK) tc_commit(kv_empty(vs));
                 if (has_next) {
                     if (walk_act(1, e + 1)) {
                         issue_qk(1, ks);
