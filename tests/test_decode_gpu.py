@@ -220,6 +220,8 @@ def team_size(S, Hq, Hkv, d, bs, lens):
     (1, 8, 2, 128, [9000], 4),                              # 71 chunks: the merge's long path
     (5, 8, 2, 128, [0, 1, 5, 17, 33], 4),                   # fewer sub-pages than warps per item
     (3, 64, 2, 128, [700, 1300, 90], 4),                    # 32 query heads per kv head: 2 groups
+    (2, 32, 8, 128, [4000, 3000], 2),                       # 32 chunks: a slice's merge in two load groups
+    (4, 4, 1, 128, [36000, 37000, 39000, 40000], 1),        # 313 chunks: a whole row's merge, long path
 ])
 def test_warp_teams(oracle, S, Hq, Hkv, d, lens, want_T):
     """Items shared by T warps of a block (sub-pages dealt round-robin, partials combined in
