@@ -4,7 +4,6 @@ bf16 inputs and block index; bitwise agreement with attn_fwd when every block is
 indices reported in the device error word."""
 import math
 
-import numpy as np
 import pytest
 import torch
 

@@ -1,7 +1,6 @@
 """GPU: the host-buffer entry points (attn_fwd_host, attn_decode_host) give bitwise the
 results of attn_fwd / attn_decode, for pinned and pageable host memory, every chunking,
 GQA, several batch entries, and on a side stream."""
-import math
 
 import pytest
 import torch
